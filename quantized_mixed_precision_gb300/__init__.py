@@ -1,0 +1,233 @@
+"""Thin Python binding of libbq.so (the C ABI declared in include/bq.h).
+
+Argument marshalling only: every function checks the torch tensors it is
+given, passes their device pointers, sizes and the current CUDA stream to
+the C entry point of the same name, and raises ``BqError`` on a non-OK
+status.  All arithmetic runs in the library's CUDA kernels; there is no
+CPU fallback -- if the library is not built, importing the binding works
+but every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libbq.so")
+HEADER = os.path.join(os.path.dirname(PKG_DIR), "include", "bq.h")
+
+BQ_OK, BQ_ERR_INVALID_ARG, BQ_ERR_UNSUPPORTED, BQ_ERR_ALIGNMENT, BQ_ERR_CUDA, BQ_ERR_TIMEOUT = range(6)
+BQ_F16, BQ_F32 = 0, 1
+LAYOUT_PLAIN, LAYOUT_INTERLEAVED = 0, 1
+ROUND_F32DIV, ROUND_BMINF_HALF = 0, 1
+LAYOUTS = {"plain": LAYOUT_PLAIN, "interleaved": LAYOUT_INTERLEAVED}
+
+_c_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+
+_SIGNATURES = {
+    "bq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "bq_quantize_sym": (ctypes.c_int, [_vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int, ctypes.c_int,
+                                       _vp, _vp, _vp]),
+    "bq_packed_size": (ctypes.c_size_t, [_c_i64, _c_i64, ctypes.c_int, ctypes.c_int]),
+    "bq_pack_weights": (ctypes.c_int, [_vp, _c_i64, _c_i64, ctypes.c_int, ctypes.c_int, _vp, _vp]),
+    "bq_gemm_i8xi8": (ctypes.c_int, [_vp, _vp, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp]),
+    "bq_gemm_i8xi4": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp]),
+    "bq_gemm_i8xi2": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp]),
+    "bq_gemm_f16xi4": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp]),
+    "bq_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+    "bq_set_wait_timeout_ns": (_c_i64, [_c_i64]),
+}
+
+_lib = None
+
+
+class BqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {bq_status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libbq.so once; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libbq.so is not built ({LIB_PATH}); run quantized_mixed_precision_gb300.build")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/bq.h declares."""
+    with open(HEADER, encoding="utf-8") as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\*?\s+\*?(bq_\w+)\s*\(", text, re.M)))
+
+
+def bq_status_string(status: int) -> str:
+    return lib().bq_status_string(status).decode()
+
+
+def _check(status: int, where: str):
+    if status != BQ_OK:
+        raise BqError(status, where)
+
+
+# ----------------------------------------------------------------------------
+# torch marshalling helpers
+# ----------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, ndim=None):
+    torch = _torch()
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _layout(layout):
+    return LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+
+
+# ----------------------------------------------------------------------------
+# Entry points
+# ----------------------------------------------------------------------------
+def bq_quantize_sym(x, bits=8, mode=ROUND_F32DIV, q=None, scale=None, stream=None):
+    """Per-row symmetric quantisation of a 2-D fp16/fp32 CUDA tensor -> (int8 codes, fp16 scale)."""
+    torch = _torch()
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    xtype = {torch.float16: BQ_F16, torch.float32: BQ_F32}[x.dtype]
+    rows, cols = x.shape
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.int8, device=x.device)
+    if scale is None:
+        scale = torch.empty((rows,), dtype=torch.float16, device=x.device)
+    _need(q, torch.int8, "q", 2)
+    _need(scale, torch.float16, "scale", 1)
+    st = lib().bq_quantize_sym(_ptr(x), xtype, rows, cols, x.stride(0), int(bits), int(mode), _ptr(q),
+                               _ptr(scale), _stream(stream))
+    _check(st, "bq_quantize_sym")
+    return q, scale
+
+
+def bq_packed_size(n, k, bits, layout=LAYOUT_INTERLEAVED) -> int:
+    return int(lib().bq_packed_size(int(n), int(k), int(bits), _layout(layout)))
+
+
+def bq_pack_weights(q, bits, layout=LAYOUT_INTERLEAVED, out=None, stream=None):
+    """Pack int8 codes (n, k) into (n, k*bits/8) bytes."""
+    torch = _torch()
+    _need(q, torch.int8, "q", 2)
+    n, k = q.shape
+    lay = _layout(layout)
+    if out is None:
+        out = torch.empty((n, k * bits // 8), dtype=torch.uint8, device=q.device)
+    _need(out, torch.uint8, "out")
+    st = lib().bq_pack_weights(_ptr(q), n, k, int(bits), lay, _ptr(out), _stream(stream))
+    _check(st, "bq_pack_weights")
+    return out
+
+
+def _gemm_out(M, N, scaled, out, device):
+    torch = _torch()
+    dtype = torch.float16 if scaled else torch.int32
+    if out is None:
+        out = torch.empty((M, N), dtype=dtype, device=device)
+    _need(out, dtype, "out", 2)
+    return out
+
+
+def bq_gemm_i8xi8(A, B, row_scale=None, col_scale=None, out=None, stream=None):
+    torch = _torch()
+    _need(A, torch.int8, "A", 2)
+    _need(B, torch.int8, "B", 2)
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("K mismatch")
+    out = _gemm_out(M, N, col_scale is not None, out, A.device)
+    st = lib().bq_gemm_i8xi8(_ptr(A), _ptr(B), M, N, K, _ptr(row_scale), _ptr(col_scale), _ptr(out),
+                             _stream(stream))
+    _check(st, "bq_gemm_i8xi8")
+    return out
+
+
+def _gemm_packed(fn_name, bits, A, Bp, layout, row_scale, col_scale, out, stream):
+    torch = _torch()
+    _need(A, torch.int8, "A", 2)
+    _need(Bp, torch.uint8, "Bp", 2)
+    M, K = A.shape
+    N = Bp.shape[0]
+    if Bp.shape[1] * 8 != K * bits:
+        raise ValueError("packed width does not match K")
+    out = _gemm_out(M, N, col_scale is not None, out, A.device)
+    st = getattr(lib(), fn_name)(_ptr(A), _ptr(Bp), _layout(layout), M, N, K, _ptr(row_scale), _ptr(col_scale),
+                                 _ptr(out), _stream(stream))
+    _check(st, fn_name)
+    return out
+
+
+def bq_gemm_i8xi4(A, Bp, layout=LAYOUT_INTERLEAVED, row_scale=None, col_scale=None, out=None, stream=None):
+    return _gemm_packed("bq_gemm_i8xi4", 4, A, Bp, layout, row_scale, col_scale, out, stream)
+
+
+def bq_gemm_i8xi2(A, Bp, layout=LAYOUT_INTERLEAVED, row_scale=None, col_scale=None, out=None, stream=None):
+    return _gemm_packed("bq_gemm_i8xi2", 2, A, Bp, layout, row_scale, col_scale, out, stream)
+
+
+def bq_gemm_f16xi4(X, Wp, col_scale, layout=LAYOUT_INTERLEAVED, out=None, stream=None):
+    torch = _torch()
+    _need(X, torch.float16, "X", 2)
+    _need(Wp, torch.uint8, "Wp", 2)
+    _need(col_scale, torch.float16, "col_scale", 1)
+    M, K = X.shape
+    N = Wp.shape[0]
+    if Wp.shape[1] * 2 != K:
+        raise ValueError("packed width does not match K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    _need(out, torch.float16, "out", 2)
+    st = lib().bq_gemm_f16xi4(_ptr(X), _ptr(Wp), _layout(layout), M, N, K, _ptr(col_scale), _ptr(out),
+                              _stream(stream))
+    _check(st, "bq_gemm_f16xi4")
+    return out
+
+
+def bq_device_status(reset=True) -> int:
+    v = ctypes.c_int(0)
+    _check(lib().bq_device_status(ctypes.byref(v), 1 if reset else 0), "bq_device_status")
+    return v.value
+
+
+def bq_set_wait_timeout_ns(ns: int) -> int:
+    return int(lib().bq_set_wait_timeout_ns(int(ns)))

@@ -1,0 +1,163 @@
+// C ABI of libbq.so (declared in include/bq.h): host-side validation and the
+// M-bucket dispatch between the skinny-M kernels and the tensor-core GEMM.
+// Nothing here allocates device memory.
+#include <atomic>
+#include <cstdint>
+
+#include "bq_internal.h"
+
+namespace bq {
+
+namespace {
+std::atomic<int64_t> g_wait_timeout_ns{2000000000LL};
+
+constexpr int64_t MAX_K = 65536;
+constexpr int64_t MAX_DIM = 1LL << 24;
+constexpr int64_t SKINNY_M = 16;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BQ_OK : BQ_ERR_CUDA; }
+
+inline bool valid_bits(int bits) { return bits == 8 || bits == 4 || bits == 2; }
+
+inline bool valid_layout(int layout) { return layout == BQ_LAYOUT_PLAIN || layout == BQ_LAYOUT_INTERLEAVED; }
+
+// Shared checks of the GEMM entry points.  max_k bounds K so that every
+// partial sum of the integer paths stays below 2**24 (exact fp32 accumulation).
+bq_status check_gemm(const void* a, const void* b, int64_t M, int64_t N, int64_t K, const void* row_scale,
+                     const void* col_scale, const void* c, int64_t max_k) {
+  if (M < 0 || N < 0 || K < 0) return BQ_ERR_INVALID_ARG;
+  if (row_scale && !col_scale) return BQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return BQ_OK;
+  // with K == 0 the operands hold no elements and may be null
+  if (!c || (K > 0 && (!a || !b))) return BQ_ERR_INVALID_ARG;
+  if (K % 64 != 0 || N % 64 != 0 || K > max_k || M > MAX_DIM || N > MAX_DIM) return BQ_ERR_UNSUPPORTED;
+  if (!aligned16(c) || (K > 0 && (!aligned16(a) || !aligned16(b)))) return BQ_ERR_ALIGNMENT;
+  if ((row_scale && !aligned16(row_scale)) || (col_scale && !aligned16(col_scale))) return BQ_ERR_ALIGNMENT;
+  return BQ_OK;
+}
+
+bq_status run_gemm(GemmArgs g, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (g.M == 0 || g.N == 0) return BQ_OK;
+  g.epi = g.col_scale ? (g.row_scale ? EPI_F16_ROWCOL : EPI_F16_COL) : EPI_I32;
+  if (g.K == 0) {
+    const size_t bytes = (size_t)g.M * (size_t)g.N * (g.epi == EPI_I32 ? 4 : 2);
+    return from_cuda(cudaMemsetAsync(g.c, 0, bytes, s));
+  }
+  cudaError_t e;
+  if (g.act == ACT_I8 && g.bbits == 8) {
+    const bool tc_ok = g.M > SKINNY_M && (g.epi != EPI_I32 || g.K <= 4096);
+    e = tc_ok ? launch_gemm_tc(g, s) : launch_gemm_dp4a(g, s);
+  } else if (g.M <= SKINNY_M) {
+    e = launch_gemv_mma(g, s);
+  } else {
+    e = launch_gemm_tc(g, s);
+  }
+  return from_cuda(e);
+}
+
+}  // namespace
+
+int64_t wait_timeout_ns() { return g_wait_timeout_ns.load(); }
+
+}  // namespace bq
+
+using namespace bq;
+
+extern "C" {
+
+const char* bq_status_string(int status) {
+  switch (status) {
+    case BQ_OK: return "BQ_OK";
+    case BQ_ERR_INVALID_ARG: return "BQ_ERR_INVALID_ARG";
+    case BQ_ERR_UNSUPPORTED: return "BQ_ERR_UNSUPPORTED";
+    case BQ_ERR_ALIGNMENT: return "BQ_ERR_ALIGNMENT";
+    case BQ_ERR_CUDA: return "BQ_ERR_CUDA";
+    case BQ_ERR_TIMEOUT: return "BQ_ERR_TIMEOUT";
+    default: return "BQ_ERR_UNKNOWN";
+  }
+}
+
+bq_status bq_quantize_sym(const void* x, int xtype, int64_t rows, int64_t cols, int64_t ld_x, int bits, int mode,
+                          int8_t* q, uint16_t* scale, void* stream) {
+  if (rows < 0 || cols < 0 || ld_x < cols) return BQ_ERR_INVALID_ARG;
+  if (!valid_bits(bits) || (xtype != BQ_F16 && xtype != BQ_F32)) return BQ_ERR_INVALID_ARG;
+  if (mode != BQ_ROUND_F32DIV && mode != BQ_ROUND_BMINF_HALF) return BQ_ERR_INVALID_ARG;
+  if (rows == 0) return BQ_OK;
+  if (!x || !q || !scale) return BQ_ERR_INVALID_ARG;
+  if (cols > MAX_DIM || rows > (1LL << 31) - 1) return BQ_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return BQ_ERR_ALIGNMENT;
+  return from_cuda(launch_quantize(x, xtype, rows, cols, ld_x, bits, mode, q, scale,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+size_t bq_packed_size(int64_t n, int64_t k, int bits, int layout) {
+  if (n < 0 || k < 0 || !valid_bits(bits) || !valid_layout(layout)) return 0;
+  const int64_t unit = (layout == BQ_LAYOUT_INTERLEAVED && bits != 8) ? 32 / bits : 8 / bits;
+  if (k % unit != 0) return 0;
+  return (size_t)n * (size_t)k * (size_t)bits / 8;
+}
+
+bq_status bq_pack_weights(const int8_t* q, int64_t n, int64_t k, int bits, int layout, uint8_t* packed,
+                          void* stream) {
+  if (n < 0 || k < 0 || !valid_bits(bits) || !valid_layout(layout)) return BQ_ERR_INVALID_ARG;
+  if (n == 0 || k == 0) return BQ_OK;
+  if (!q || !packed) return BQ_ERR_INVALID_ARG;
+  if (bq_packed_size(n, k, bits, layout) == 0) return BQ_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(packed)) return BQ_ERR_ALIGNMENT;
+  return from_cuda(launch_pack(q, n, k, bits, layout, packed, static_cast<cudaStream_t>(stream)));
+}
+
+bq_status bq_gemm_i8xi8(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
+                        const uint16_t* row_scale, const uint16_t* col_scale, void* C, void* stream) {
+  bq_status st = check_gemm(A, B, M, N, K, row_scale, col_scale, C, MAX_K);
+  if (st != BQ_OK) return st;
+  GemmArgs g{A, B, ACT_I8, 8, BQ_LAYOUT_PLAIN, M, N, K, row_scale, col_scale, EPI_I32, C};
+  return run_gemm(g, stream);
+}
+
+static bq_status gemm_sub_byte(const int8_t* A, const uint8_t* Bp, int layout, int bits, int64_t M, int64_t N,
+                               int64_t K, const uint16_t* row_scale, const uint16_t* col_scale, void* C,
+                               void* stream) {
+  if (!valid_layout(layout)) return BQ_ERR_INVALID_ARG;
+  // |a * b| <= 128 * 8 (4 bits) or 128 * 2 (2 bits): K <= 2**24 / that keeps sums exact
+  const int64_t max_k = bits == 4 ? 16384 : MAX_K;
+  bq_status st = check_gemm(A, Bp, M, N, K, row_scale, col_scale, C, max_k);
+  if (st != BQ_OK) return st;
+  GemmArgs g{A, Bp, ACT_I8, bits, layout, M, N, K, row_scale, col_scale, EPI_I32, C};
+  return run_gemm(g, stream);
+}
+
+bq_status bq_gemm_i8xi4(const int8_t* A, const uint8_t* Bp, int layout, int64_t M, int64_t N, int64_t K,
+                        const uint16_t* row_scale, const uint16_t* col_scale, void* C, void* stream) {
+  return gemm_sub_byte(A, Bp, layout, 4, M, N, K, row_scale, col_scale, C, stream);
+}
+
+bq_status bq_gemm_i8xi2(const int8_t* A, const uint8_t* Bp, int layout, int64_t M, int64_t N, int64_t K,
+                        const uint16_t* row_scale, const uint16_t* col_scale, void* C, void* stream) {
+  return gemm_sub_byte(A, Bp, layout, 2, M, N, K, row_scale, col_scale, C, stream);
+}
+
+bq_status bq_gemm_f16xi4(const uint16_t* X, const uint8_t* Wp, int layout, int64_t M, int64_t N, int64_t K,
+                         const uint16_t* col_scale, uint16_t* Y, void* stream) {
+  if (!valid_layout(layout)) return BQ_ERR_INVALID_ARG;
+  if (M > 0 && N > 0 && !col_scale) return BQ_ERR_INVALID_ARG;
+  bq_status st = check_gemm(X, Wp, M, N, K, nullptr, col_scale, Y, MAX_K);
+  if (st != BQ_OK) return st;
+  GemmArgs g{X, Wp, ACT_F16, 4, layout, M, N, K, nullptr, col_scale, EPI_F16_COL, Y};
+  return run_gemm(g, stream);
+}
+
+bq_status bq_device_status(int* status_out, int reset) {
+  if (!status_out) return BQ_ERR_INVALID_ARG;
+  return from_cuda(read_device_status(status_out, reset != 0));
+}
+
+int64_t bq_set_wait_timeout_ns(int64_t ns) {
+  if (ns < 0) ns = 0;
+  return g_wait_timeout_ns.exchange(ns);
+}
+
+}  // extern "C"

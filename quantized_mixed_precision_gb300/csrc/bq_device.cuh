@@ -1,0 +1,264 @@
+// Device-side helpers shared by the bq kernels: fp16 conversions of packed
+// integer codes, mbarrier waits with a time limit, and thin inline-PTX
+// wrappers for the sm_100-family tensor-core instructions (tcgen05.*).
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "bq_internal.h"
+
+namespace bq {
+
+// ---------------------------------------------------------------------------
+// Device status word: the first error recorded by a kernel (BQ_OK if none).
+// The word lives in the tensor-core GEMM's translation unit; kernels receive
+// its address as an argument.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void record_error(int* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// Exact integer -> fp16 conversions by exponent-bias ("magic number")
+// arithmetic: a field value u in [0, 2^b) OR'ed into the low mantissa bits of
+// 1024.0 (0x6400) gives the fp16 number 1024 + u exactly; subtracting
+// 1024 + bias yields the signed value.  Two's-complement fields are first
+// made offset-binary by flipping their top bit (XOR), so u = v + bias.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
+  uint32_t r;
+  // (a & mask) | magic
+  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(a), "r"(mask), "r"(magic));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// fp16x2 constants (low half, high half equal)
+constexpr uint32_t H2_MAGIC = 0x64006400u;      // 1024.0
+constexpr uint32_t H2_1032 = 0x64086408u;       // 1024 + 8
+constexpr uint32_t H2_1152 = 0x64806480u;       // 1024 + 128
+constexpr uint32_t H2_1026 = 0x64026402u;       // 1024 + 2
+constexpr uint32_t H2_INV16 = 0x2c002c00u;      // 1/16
+constexpr uint32_t H2_NEG72 = 0xd480d480u;      // -(64 + 8)
+constexpr uint32_t H2_INV4 = 0x34003400u;       // 1/4
+constexpr uint32_t H2_NEG258 = 0xdc08dc08u;     // -(256 + 2)
+constexpr uint32_t H2_NEG66 = 0xd420d420u;      // -(64 + 2)
+constexpr uint32_t H2_INV64 = 0x24002400u;      // 1/64
+constexpr uint32_t H2_NEG18 = 0xcc80cc80u;      // -(16 + 2)
+
+// 4 int8 (one 32-bit word, k order 0..3) -> 2 fp16x2 words: (k0,k1), (k2,k3).
+__device__ __forceinline__ void cvt_i8x4_f16(uint32_t w, uint32_t& h01, uint32_t& h23) {
+  const uint32_t u = w ^ 0x80808080u;            // offset binary: u = v + 128
+  // bytes {u.b0, 0x64, u.b1, 0x64} and {u.b2, 0x64, u.b3, 0x64}
+  h01 = hsub2_u32(prmt(u, 0x64646464u, 0x5140u), H2_1152);
+  h23 = hsub2_u32(prmt(u, 0x64646464u, 0x5342u), H2_1152);
+}
+
+// One interleaved 4-bit word (8 codes) -> 4 fp16x2 words in k order.
+// Field positions 0..3 hold k = 0, 2, 4, 6 and positions 4..7 hold k = 1, 3, 5, 7.
+__device__ __forceinline__ void cvt_i4x8_f16(uint32_t w, uint32_t (&h)[4]) {
+  const uint32_t x = w ^ 0x88888888u;            // u = v + 8
+  const uint32_t y = x >> 8;
+  h[0] = hsub2_u32(lop3_and_or(x, 0x000f000fu, H2_MAGIC), H2_1032);                 // k0, k1
+  h[1] = hfma2_u32(lop3_and_or(x, 0x00f000f0u, H2_MAGIC), H2_INV16, H2_NEG72);      // k2, k3
+  h[2] = hsub2_u32(lop3_and_or(y, 0x000f000fu, H2_MAGIC), H2_1032);                 // k4, k5
+  h[3] = hfma2_u32(lop3_and_or(y, 0x00f000f0u, H2_MAGIC), H2_INV16, H2_NEG72);      // k6, k7
+}
+
+// One interleaved 2-bit word (16 codes) -> 8 fp16x2 words in k order.
+// Field positions 0..7 hold k = 0, 2, ..., 14 and positions 8..15 hold k = 1, 3, ..., 15.
+__device__ __forceinline__ void cvt_i2x16_f16(uint32_t w, uint32_t (&h)[8]) {
+  const uint32_t x = w ^ 0xaaaaaaaau;            // u = v + 2
+  const uint32_t y = x >> 8;
+  h[0] = hsub2_u32(lop3_and_or(x, 0x00030003u, H2_MAGIC), H2_1026);
+  h[1] = hfma2_u32(lop3_and_or(x, 0x000c000cu, H2_MAGIC), H2_INV4, H2_NEG258);
+  h[2] = hfma2_u32(lop3_and_or(x, 0x00300030u, H2_MAGIC), H2_INV16, H2_NEG66);
+  h[3] = hfma2_u32(lop3_and_or(x, 0x00c000c0u, H2_MAGIC), H2_INV64, H2_NEG18);
+  h[4] = hsub2_u32(lop3_and_or(y, 0x00030003u, H2_MAGIC), H2_1026);
+  h[5] = hfma2_u32(lop3_and_or(y, 0x000c000cu, H2_MAGIC), H2_INV4, H2_NEG258);
+  h[6] = hfma2_u32(lop3_and_or(y, 0x00300030u, H2_MAGIC), H2_INV16, H2_NEG66);
+  h[7] = hfma2_u32(lop3_and_or(y, 0x00c000c0u, H2_MAGIC), H2_INV64, H2_NEG18);
+}
+
+// Plain-layout sub-byte word -> interleaved word (register permutation), so
+// the same converters serve both layouts.
+__device__ __forceinline__ uint32_t plain_to_inter_i4(uint32_t w) {
+  // plain nibble i holds k = i.  Want positions 0..3 <- k0,k2,k4,k6 and 4..7 <- k1,k3,k5,k7.
+  uint32_t even = 0, odd = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    even |= ((w >> (8 * i)) & 0xfu) << (4 * i);
+    odd |= ((w >> (8 * i + 4)) & 0xfu) << (4 * i);
+  }
+  return even | (odd << 16);
+}
+
+__device__ __forceinline__ uint32_t plain_to_inter_i2(uint32_t w) {
+  uint32_t even = 0, odd = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    even |= ((w >> (4 * i)) & 0x3u) << (2 * i);
+    odd |= ((w >> (4 * i + 2)) & 0x3u) << (2 * i);
+  }
+  return even | (odd << 16);
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory mbarriers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with the given parity has completed, or give up after
+// timeout_ns nanoseconds: records BQ_ERR_TIMEOUT in *status, returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 >= timeout_ns) {
+      record_error(status, BQ_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor core) wrappers, cta_group::1
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (fp16 or bf16 operands, fp32 accumulator).
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on an mbarrier when all previously issued tcgen05 ops of this thread complete.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives lane (base + i).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile stored in the
+// 128-byte swizzle layout: rows of 128 bytes (64 fp16 along K), 8-row groups
+// of 1024 bytes; inside a group, 16-byte chunk c of row r sits at chunk
+// position c ^ r.  The tile base must be 1024-byte aligned.  Advancing K by
+// 16 elements inside the 128-byte row is done by adding 32 bytes to the
+// start address (the swizzle is applied on absolute address bits).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3ffffu) >> 4);            // start address
+  d |= (uint64_t)1 << 16;                              // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;                    // stride byte offset: 8-row group pitch
+  d |= (uint64_t)1 << 46;                              // descriptor version (sm_100 family)
+  d |= (uint64_t)2 << 61;                              // swizzle mode: 128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
+  return (1u << 4)                         // D format: f32
+         | (0u << 7) | (0u << 10)          // A, B format: f16
+         | ((uint32_t)(n >> 3) << 17)      // N / 8
+         | ((uint32_t)(m >> 4) << 24);     // M / 16
+}
+
+}  // namespace bq

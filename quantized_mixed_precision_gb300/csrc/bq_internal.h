@@ -1,0 +1,51 @@
+// Internal launchers behind the C ABI (include/bq.h).  Every launcher takes
+// already validated arguments and enqueues work on `stream`; it returns the
+// CUDA error of the launch.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/bq.h"
+
+namespace bq {
+
+// Time limit of bounded device-side waits (nanoseconds).
+int64_t wait_timeout_ns();
+// Address (on the current device) of the status word the bounded waits write.
+cudaError_t device_status_ptr(int** out);
+// Synchronise the device, read the status word and optionally clear it.
+cudaError_t read_device_status(int* status_out, bool reset);
+
+cudaError_t launch_quantize(const void* x, int xtype, int64_t rows, int64_t cols, int64_t ld_x, int bits,
+                            int mode, int8_t* q, uint16_t* scale, cudaStream_t stream);
+
+cudaError_t launch_pack(const int8_t* q, int64_t n, int64_t k, int bits, int layout, uint8_t* packed,
+                        cudaStream_t stream);
+
+// Epilogue kinds shared by the GEMM kernels.
+enum EpiKind : int { EPI_I32 = 0, EPI_F16_COL = 1, EPI_F16_ROWCOL = 2 };
+// Activation operand kinds.
+enum ActKind : int { ACT_I8 = 0, ACT_F16 = 1 };
+
+struct GemmArgs {
+  const void* a;          // activations (M, K): int8 or fp16
+  const void* b;          // weights (N, K): int8 or packed 4/2-bit
+  int act;                // ActKind
+  int bbits;              // 8, 4, 2
+  int layout;             // bq_layout of b (sub-byte only)
+  int64_t M, N, K;
+  const uint16_t* row_scale;  // fp16 (M) or null
+  const uint16_t* col_scale;  // fp16 (N) or null
+  int epi;                // EpiKind
+  void* c;                // int32 or fp16 (M, N)
+};
+
+// Skinny-M path (M <= 16): one pass over the weights, legacy mma.sync fp16.
+cudaError_t launch_gemv_mma(const GemmArgs& g, cudaStream_t stream);
+// int8 x int8 with exact int32 dp4a accumulation (any M).
+cudaError_t launch_gemm_dp4a(const GemmArgs& g, cudaStream_t stream);
+// Tensor-core (tcgen05) GEMM for larger M.
+cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream);
+
+}  // namespace bq

@@ -1,0 +1,126 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+the header declares, and rejects invalid calls on the host before any launch.
+
+Only calls that fail validation are made here (fake but aligned pointers are
+never dereferenced because validation returns first)."""
+
+import ctypes
+import os
+
+import pytest
+
+import quantized_mixed_precision_gb300 as bq
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(bq.LIB_PATH):
+        from quantized_mixed_precision_gb300 import build
+        build.build()
+    return bq.lib()
+
+
+EXPECTED = sorted([
+    "bq_status_string", "bq_quantize_sym", "bq_packed_size", "bq_pack_weights", "bq_gemm_i8xi8",
+    "bq_gemm_i8xi4", "bq_gemm_i8xi2", "bq_gemm_f16xi4", "bq_device_status", "bq_set_wait_timeout_ns",
+])
+
+FAKE = ctypes.c_void_p(0x10000)     # aligned, never dereferenced
+FAKE_ODD = ctypes.c_void_p(0x10008)  # 8-byte aligned only
+
+
+def test_header_lists_expected_functions():
+    assert bq.header_functions() == EXPECTED
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in bq.header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert bq.bq_status_string(0) == "BQ_OK"
+    assert bq.bq_status_string(5) == "BQ_ERR_TIMEOUT"
+    assert bq.bq_status_string(99) == "BQ_ERR_UNKNOWN"
+
+
+def test_packed_size(lib):
+    assert bq.bq_packed_size(11008, 4096, 4, "interleaved") == 22544384
+    assert bq.bq_packed_size(8192, 8192, 2, "plain") == 16 * 2 ** 20
+    assert bq.bq_packed_size(4, 6, 4, "plain") == 12
+    assert bq.bq_packed_size(4, 12, 4, "interleaved") == 0      # needs k % 8
+    assert bq.bq_packed_size(4, 16, 3, "plain") == 0
+    assert bq.bq_packed_size(-1, 16, 4, "plain") == 0
+
+
+def test_quantize_validation(lib):
+    f = lib.bq_quantize_sym
+    assert f(None, 0, 4, 8, 8, 8, 0, FAKE, FAKE, None) == bq.BQ_ERR_INVALID_ARG
+    assert f(FAKE, 0, 4, 8, 4, 8, 0, FAKE, FAKE, None) == bq.BQ_ERR_INVALID_ARG     # ld_x < cols
+    assert f(FAKE, 0, 4, 8, 8, 3, 0, FAKE, FAKE, None) == bq.BQ_ERR_INVALID_ARG     # bits
+    assert f(FAKE, 2, 4, 8, 8, 8, 0, FAKE, FAKE, None) == bq.BQ_ERR_INVALID_ARG     # xtype
+    assert f(FAKE, 0, 4, 8, 8, 8, 7, FAKE, FAKE, None) == bq.BQ_ERR_INVALID_ARG     # mode
+    assert f(FAKE_ODD, 0, 4, 8, 8, 8, 0, FAKE, FAKE, None) == bq.BQ_ERR_ALIGNMENT
+    assert f(FAKE, 0, 4, 1 << 25, 1 << 25, 8, 0, FAKE, FAKE, None) == bq.BQ_ERR_UNSUPPORTED
+    assert f(None, 0, 0, 8, 8, 8, 0, None, None, None) == bq.BQ_OK                  # empty
+
+
+def test_pack_validation(lib):
+    f = lib.bq_pack_weights
+    assert f(None, 4, 64, 4, 1, FAKE, None) == bq.BQ_ERR_INVALID_ARG
+    assert f(FAKE, 4, 64, 5, 1, FAKE, None) == bq.BQ_ERR_INVALID_ARG
+    assert f(FAKE, 4, 64, 4, 2, FAKE, None) == bq.BQ_ERR_INVALID_ARG
+    assert f(FAKE, 4, 12, 4, 1, FAKE, None) == bq.BQ_ERR_UNSUPPORTED
+    assert f(FAKE, 4, 64, 4, 1, FAKE_ODD, None) == bq.BQ_ERR_ALIGNMENT
+    assert f(FAKE, 0, 64, 4, 1, FAKE, None) == bq.BQ_OK
+
+
+@pytest.mark.parametrize("name", ["bq_gemm_i8xi4", "bq_gemm_i8xi2"])
+def test_packed_gemm_validation(lib, name):
+    f = getattr(lib, name)
+    ok = dict(A=FAKE, B=FAKE, L=1, M=32, N=64, K=64, rs=None, cs=FAKE, C=FAKE)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["A"], a["B"], a["L"], a["M"], a["N"], a["K"], a["rs"], a["cs"], a["C"], None)
+
+    assert call(A=None) == bq.BQ_ERR_INVALID_ARG
+    assert call(C=None) == bq.BQ_ERR_INVALID_ARG
+    assert call(L=5) == bq.BQ_ERR_INVALID_ARG
+    assert call(M=-1) == bq.BQ_ERR_INVALID_ARG
+    assert call(rs=FAKE, cs=None) == bq.BQ_ERR_INVALID_ARG
+    assert call(K=96) == bq.BQ_ERR_UNSUPPORTED
+    assert call(N=96) == bq.BQ_ERR_UNSUPPORTED
+    assert call(K=1 << 17) == bq.BQ_ERR_UNSUPPORTED
+    assert call(A=FAKE_ODD) == bq.BQ_ERR_ALIGNMENT
+    assert call(cs=FAKE_ODD) == bq.BQ_ERR_ALIGNMENT
+    assert call(M=0) == bq.BQ_OK
+    assert call(N=0, C=None) == bq.BQ_OK
+
+
+def test_i8xi4_exactness_bound(lib):
+    # 128 * 8 * K must stay <= 2**24: K = 16384 is accepted by validation,
+    # 16448 is not (the i8xi2 bound is 65536).
+    f = lib.bq_gemm_i8xi4
+    assert f(FAKE, FAKE, 1, 32, 64, 16448, None, None, FAKE, None) == bq.BQ_ERR_UNSUPPORTED
+    g = lib.bq_gemm_i8xi2
+    assert g(FAKE, FAKE, 1, 32, 64, 65600, None, None, FAKE, None) == bq.BQ_ERR_UNSUPPORTED
+
+
+def test_i8xi8_and_f16xi4_validation(lib):
+    f = lib.bq_gemm_i8xi8
+    assert f(None, FAKE, 4, 64, 64, None, None, FAKE, None) == bq.BQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 4, 64, 100, None, None, FAKE, None) == bq.BQ_ERR_UNSUPPORTED
+    g = lib.bq_gemm_f16xi4
+    assert g(FAKE, FAKE, 1, 4, 64, 64, None, FAKE, None) == bq.BQ_ERR_INVALID_ARG   # scale required
+    assert g(FAKE, FAKE, 1, 4, 64, 64, FAKE, FAKE_ODD, None) == bq.BQ_ERR_ALIGNMENT
+    assert g(FAKE, FAKE, 0, 0, 64, 64, None, None, None) == bq.BQ_OK
+
+
+def test_device_status_null(lib):
+    assert lib.bq_device_status(None, 0) == bq.BQ_ERR_INVALID_ARG
+
+
+def test_wait_timeout_setter(lib):
+    old = bq.bq_set_wait_timeout_ns(12345)
+    assert bq.bq_set_wait_timeout_ns(old) == 12345

@@ -1,0 +1,275 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Integer results (codes, packed bytes, int32 accumulators) must match bit for
+bit.  fp16 results must satisfy |y - y_ref| <= max(1e-3 |y_ref|, 1e-3 * s_ij)
+where s_ij is the dequantisation scale of the element (per-column scale, or
+row scale times column scale), and infinities must match exactly.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+import quantized_mixed_precision_gb300 as bq  # noqa: E402
+from oracle import bq_oracle as O  # noqa: E402
+from quantized_mixed_precision_gb300 import workloads as W  # noqa: E402
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    bq.lib()
+    yield
+    torch.cuda.synchronize()
+    assert bq.bq_device_status(reset=True) == bq.BQ_OK
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def host(t):
+    return t.cpu().numpy()
+
+
+def assert_f16_close(y, y_ref, scale_ij, what=""):
+    y = y.astype(np.float64)
+    y_ref = y_ref.astype(np.float64)
+    inf_ref = ~np.isfinite(y_ref)
+    assert (np.isfinite(y) == ~inf_ref).all(), f"{what}: inf pattern differs"
+    assert (y[inf_ref] == y_ref[inf_ref]).all(), f"{what}: inf sign differs"
+    fin = ~inf_ref
+    tol = np.maximum(1e-3 * np.abs(y_ref), 1e-3 * np.broadcast_to(scale_ij, y_ref.shape).astype(np.float64))
+    err = np.abs(y - y_ref)
+    bad = fin & (err > tol)
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; "
+                           f"worst err/tol {np.max(err[fin] / tol[fin]):.3g}")
+
+
+# ---------------------------------------------------------------------------
+# quantiser
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("rows,cols", [(1, 8), (7, 40), (33, 256), (100, 1000), (5, 4096), (3, 5000), (2, 3)])
+@pytest.mark.parametrize("bits", [8, 4, 2])
+@pytest.mark.parametrize("mode", [bq.ROUND_F32DIV, bq.ROUND_BMINF_HALF])
+def test_quantize_parity(rows, cols, bits, mode):
+    rng = np.random.default_rng(rows * 7 + cols)
+    x = W.normal_f16(rng, (rows, cols), 0.5)
+    if rows > 2:
+        x[1] = 0                                               # zero row
+        x[2, : min(cols, 3)] = np.float16(178 * 2.0 ** -24)    # subnormal scale, saturation
+        x[2, min(cols, 3):] = 0
+    q_ref, s_ref = O.quantize_sym(x, bits, "f32div" if mode == bq.ROUND_F32DIV else "bminf_half")
+    q, s = bq.bq_quantize_sym(dev(x), bits, mode)
+    assert (host(s).view(np.uint16) == s_ref.view(np.uint16)).all()
+    assert (host(q) == q_ref).all()
+
+
+def test_quantize_parity_f32_and_strided():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((9, 300)) * 2).astype(np.float32)
+    q_ref, s_ref = O.quantize_sym(x, 8)
+    q, s = bq.bq_quantize_sym(dev(x), 8)
+    assert (host(s).view(np.uint16) == s_ref.view(np.uint16)).all() and (host(q) == q_ref).all()
+    big = W.normal_f16(rng, (6, 512), 1.0)
+    xt = dev(big)[:, :256]                                     # leading dimension 512
+    q_ref, s_ref = O.quantize_sym(big[:, :256], 4)
+    q, s = bq.bq_quantize_sym(xt, 4)
+    assert (host(s).view(np.uint16) == s_ref.view(np.uint16)).all() and (host(q) == q_ref).all()
+
+
+def test_quantize_workload_full_size():
+    d = W.cfg1()
+    for name in ("W", "X"):
+        q_ref, s_ref = O.quantize_sym(d[name], 8)
+        q, s = bq.bq_quantize_sym(dev(d[name]), 8)
+        assert (host(s).view(np.uint16) == s_ref.view(np.uint16)).all()
+        assert (host(q) == q_ref).all()
+
+
+# ---------------------------------------------------------------------------
+# packer
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("bits", [8, 4, 2])
+@pytest.mark.parametrize("layout", ["plain", "interleaved"])
+@pytest.mark.parametrize("n,k", [(1, 64), (13, 256), (256, 4096)])
+def test_pack_parity(bits, layout, n, k):
+    rng = np.random.default_rng(n + k + bits)
+    lo = -(1 << (bits - 1))
+    q = rng.integers(lo, -lo, size=(n, k), dtype=np.int8)
+    p = bq.bq_pack_weights(dev(q), bits, layout)
+    assert (host(p) == O.pack(q, bits, layout)).all()
+
+
+def test_pack_plain_odd_width():
+    q = np.array([[1, -1, 3, -8, 7, 0]], np.int8)
+    p = bq.bq_pack_weights(dev(q), 4, "plain")
+    assert host(p)[0].tolist() == O.pack_plain(q, 4)[0].tolist()
+
+
+# ---------------------------------------------------------------------------
+# integer GEMMs (skinny and tensor-core paths, ragged M, all epilogues)
+# ---------------------------------------------------------------------------
+def _codes(rng, bits, shape):
+    return {8: W.int8_uniform, 4: W.int4_uniform, 2: W.int2_uniform}[bits](rng, shape)
+
+
+def _run_int_gemm(bits, A, Bq, layout, rs, cs):
+    if bits == 8:
+        return bq.bq_gemm_i8xi8(dev(A), dev(Bq), row_scale=rs, col_scale=cs)
+    Bp = dev(O.pack(Bq, bits, layout))
+    fn = bq.bq_gemm_i8xi4 if bits == 4 else bq.bq_gemm_i8xi2
+    return fn(dev(A), Bp, layout, row_scale=rs, col_scale=cs)
+
+
+SHAPES = [(1, 64, 64), (3, 128, 192), (16, 192, 256), (17, 256, 128), (130, 320, 512), (300, 512, 1024),
+          (256, 256, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("bits", [8, 4, 2])
+@pytest.mark.parametrize("epi", ["i32", "col", "rowcol"])
+def test_int_gemm_parity(M, N, K, bits, epi):
+    rng = np.random.default_rng(M * 31 + N * 7 + K + bits)
+    A = W.int8_uniform(rng, (M, K))
+    Bq = _codes(rng, bits, (N, K))
+    sw = W.uniform_f16(rng, (N,), 1e-3, 1e-2)
+    sx = W.uniform_f16(rng, (M,), 1e-3, 1e-1)
+    c_ref = O.gemm_int(A, Bq)
+    for layout in (["interleaved", "plain"] if bits != 8 else ["plain"]):
+        if epi == "i32":
+            c = host(_run_int_gemm(bits, A, Bq, layout, None, None))
+            assert (c == c_ref).all(), f"layout {layout}"
+        elif epi == "col":
+            y = host(_run_int_gemm(bits, A, Bq, layout, None, dev(sw)))
+            assert_f16_close(y, O.dequant(c_ref, sw), sw[None, :].astype(np.float64), f"col {layout}")
+        else:
+            y = host(_run_int_gemm(bits, A, Bq, layout, dev(sx), dev(sw)))
+            s_ij = sx[:, None].astype(np.float64) * sw[None, :].astype(np.float64)
+            assert_f16_close(y, O.dequant(c_ref, sw, sx), s_ij, f"rowcol {layout}")
+
+
+@pytest.mark.parametrize("M", [1, 40, 200])
+def test_int_gemm_extreme_values_exact(M):
+    # Largest magnitudes: -128 * -8 (4-bit, K = 16384) and -128 * -128 (int8,
+    # K = 4096 -> 2**26, beyond fp32's exact integers unless sliced).
+    K4 = 16384
+    A = np.full((M, K4), -128, np.int8)
+    B4 = np.full((64, K4), -8, np.int8)
+    c = host(bq.bq_gemm_i8xi4(dev(A), dev(O.pack(B4, 4, "interleaved")), "interleaved"))
+    assert (c == 1024 * K4).all()
+    K8 = 4096
+    A8 = np.full((M, K8), -128, np.int8)
+    A8[:, ::3] = 127
+    B8 = np.full((128, K8), -128, np.int8)
+    c8 = host(bq.bq_gemm_i8xi8(dev(A8), dev(B8)))
+    assert (c8 == O.gemm_int(A8, B8)).all()
+
+
+def test_i8xi8_int32_large_k_path():
+    rng = np.random.default_rng(21)
+    A = W.int8_uniform(rng, (70, 8192))
+    B = W.int8_uniform(rng, (128, 8192))
+    assert (host(bq.bq_gemm_i8xi8(dev(A), dev(B))) == O.gemm_int(A, B)).all()
+
+
+def test_gemm_k_zero_and_empty():
+    A = torch.empty((5, 0), dtype=torch.int8, device=DEV)
+    B = torch.empty((64, 0), dtype=torch.int8, device=DEV)
+    c = bq.bq_gemm_i8xi8(A, B)
+    assert (host(c) == 0).all()
+    A0 = torch.empty((0, 64), dtype=torch.int8, device=DEV)
+    B0 = torch.zeros((64, 64), dtype=torch.int8, device=DEV)
+    assert bq.bq_gemm_i8xi8(A0, B0).shape == (0, 64)
+
+
+# ---------------------------------------------------------------------------
+# fp16 x 4-bit
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (4, 128, 320), (16, 192, 256), (17, 64, 128), (64, 256, 512),
+                                   (200, 320, 1024)])
+@pytest.mark.parametrize("layout", ["interleaved", "plain"])
+def test_f16xi4_parity(M, N, K, layout):
+    rng = np.random.default_rng(M + N + K)
+    X = W.normal_f16(rng, (M, K), 1.0)
+    q = W.int4_uniform(rng, (N, K))
+    s = W.uniform_f16(rng, (N,), 0.008, 0.016)
+    y = host(bq.bq_gemm_f16xi4(dev(X), dev(O.pack(q, 4, layout)), dev(s), layout))
+    assert_f16_close(y, O.gemm_f16xq(X, q, s), s[None, :].astype(np.float64), "f16xi4")
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size (sampled outputs where the oracle would be slow)
+# ---------------------------------------------------------------------------
+def test_workload_int8xint4_256_int32():
+    d = W.cfg0()
+    c = bq.bq_gemm_i8xi4(dev(d["A"]), dev(O.pack(d["B"], 4, "plain")), "plain")
+    assert (host(c) == O.gemm_int(d["A"], d["B"])).all()
+
+
+def test_workload_quantize_int8xint8_1024x4096x4096():
+    d = W.cfg1()
+    xq, sx = bq.bq_quantize_sym(dev(d["X"]), 8)
+    wq, sw = bq.bq_quantize_sym(dev(d["W"]), 8)
+    y = host(bq.bq_gemm_i8xi8(xq, wq, row_scale=sx, col_scale=sw))
+    y_ref, (xq_r, sx_r, wq_r, sw_r, c_r) = O.quantized_linear_i8(d["X"], d["W"])
+    s_ij = sx_r[:, None].astype(np.float64) * sw_r[None, :].astype(np.float64)
+    assert_f16_close(y, y_ref, s_ij, "quantized linear")
+
+
+def test_workload_int8xint4_dequant_4096_sampled():
+    d = W.cfg2()
+    y = host(bq.bq_gemm_i8xi4(dev(d["A"]), dev(O.pack(d["B"], 4, "interleaved")), "interleaved",
+                              col_scale=dev(d["scale"])))
+    rows = np.r_[np.arange(0, 4096, 61), 4095]
+    y_ref = O.dequant(O.gemm_int(d["A"][rows], d["B"]), d["scale"])
+    assert_f16_close(y[rows], y_ref, d["scale"][None, :].astype(np.float64), "4096^3")
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 64, 256, 1024])
+def test_workload_f16xint4_dynamic_m(M):
+    d = W.cfg3(M=M)
+    s = O.quantize_scale(d["S"], 4)
+    Wp = dev(O.pack(d["W"], 4, "interleaved"))
+    y = host(bq.bq_gemm_f16xi4(dev(d["X"]), Wp, dev(s), "interleaved"))
+    assert_f16_close(y, O.gemm_f16xq(d["X"], d["W"], s), s[None, :].astype(np.float64), f"M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 128, 1024])
+def test_workload_int8xternary(M):
+    d = W.cfg4(M=M)
+    Bp = dev(O.pack(d["B"], 2, "interleaved"))
+    y = host(bq.bq_gemm_i8xi2(dev(d["A"]), Bp, "interleaved", col_scale=dev(d["scale"])))
+    rows = np.arange(M) if M <= 128 else np.r_[np.arange(0, M, 17), M - 1]
+    y_ref = O.dequant(O.gemm_int(d["A"][rows], d["B"]), d["scale"])
+    assert_f16_close(y[rows], y_ref, d["scale"][None, :].astype(np.float64), f"ternary M={M}")
+
+
+# ---------------------------------------------------------------------------
+# bounded waits: a wait that runs out reports BQ_ERR_TIMEOUT and the context
+# stays usable (no fault, no hang)
+# ---------------------------------------------------------------------------
+def test_wait_timeout_reports_and_recovers():
+    rng = np.random.default_rng(5)
+    A = W.int8_uniform(rng, (256, 1024))
+    B = W.int4_uniform(rng, (256, 1024))
+    Ad, Bp = dev(A), dev(O.pack(B, 4, "interleaved"))
+    torch.cuda.synchronize()
+    assert bq.bq_device_status(reset=True) == bq.BQ_OK
+    old = bq.bq_set_wait_timeout_ns(0)          # give up at the first unsuccessful poll
+    try:
+        bq.bq_gemm_i8xi4(Ad, Bp, "interleaved")
+        torch.cuda.synchronize()
+    finally:
+        bq.bq_set_wait_timeout_ns(old)
+    st = bq.bq_device_status(reset=True)
+    assert st in (bq.BQ_OK, bq.BQ_ERR_TIMEOUT)
+    c = host(bq.bq_gemm_i8xi4(Ad, Bp, "interleaved"))
+    assert (c == O.gemm_int(A, B)).all()
+    assert bq.bq_device_status(reset=True) == bq.BQ_OK
