@@ -1,0 +1,403 @@
+#!/usr/bin/env python
+"""Benchmark of the quantised mixed-precision hot path on GB300.
+
+A step is one INT8 x INT4 GEMM with the fused per-column dequantisation at
+M = N = K = 4096 (A int8 uniform in [-128, 127], B int4 uniform in [-8, 7]
+packed in the interleaved layout, fp16 scale uniform in [1e-3, 1e-2], fp16
+output), called through the library's C ABI.  Inputs are resident in HBM;
+L2 is flushed (a 512 MiB write) between timed steps, outside the timed
+events.  The same protocol measures the M = 1 fp16 x INT4 GEMV of an
+N = 11008, K = 4096 layer ("gemv") and, more briefly, the other workloads
+("paths").
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bq|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs its own copy of
+the workload (independent problems, no collective on the data path) and the
+reported value is the work of all ranks divided by the slowest rank's time.
+--impl reference times the CPU oracle (the plain definition of the method)
+on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "INT8xINT4 GEMM TOPS & f16xINT4 GEMV GB/s at 1 GB300; % of int8/HBM roofline"
+WORKLOAD = ("INT8xINT4 GEMM with fused per-column fp16 dequant, M=N=K=4096 "
+            "(A int8 U[-128,127], B int4 U[-8,7] interleaved-packed, scale fp16 U[1e-3,1e-2], C fp16), seed 0")
+GEMV_WORKLOAD = "fp16 x INT4 GEMV, M=1, N=11008, K=4096 (X fp16 N(0,1), W int4 packed, scale = absmax/7 of N(0,0.02))"
+M2 = N2 = K2 = 4096
+OPS2 = 2 * M2 * N2 * K2
+FLUSH_BYTES = 512 * 2 ** 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["bq", "reference"], default="bq")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-paths", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def source_sha(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """Per-launch DRAM traffic from the committed ncu summary, only if the
+    kernel's sources are unchanged since it was taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f).get(kernel)
+    if not t:
+        return None
+    if t.get("source_sha") != source_sha(*t["sources"]):
+        return None
+    return t.get("traffic_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.proc or not self.tmp:
+            return None
+        with open(self.tmp.name) as f:
+            rows = [r for r in csv.reader(f) if len(r) >= 9]
+        os.unlink(self.tmp.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def time_steps(torch, fn, steps, warmup, flush, stream):
+    """Per-step device time (ms) with CUDA events on the launching stream; L2
+    flushed before every step, outside the events."""
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in evs:
+        flush.zero_()
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import quantized_mixed_precision_gb300 as bq
+    from quantized_mixed_precision_gb300 import roofline, workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    bq.lib()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # ---- headline workload: INT8 x INT4 4096^3 with per-column dequant ----
+    d = W.cfg2()
+    A = torch.from_numpy(d["A"]).to(dev)
+    Bq = torch.from_numpy(d["B"]).to(dev)
+    Bp = bq.bq_pack_weights(Bq, 4, "interleaved")       # offline packing, not timed
+    sc = torch.from_numpy(d["scale"]).to(dev)
+    C = torch.empty((M2, N2), dtype=torch.float16, device=dev)
+    del Bq
+
+    def step():
+        bq.bq_gemm_i8xi4(A, Bp, "interleaved", col_scale=sc, out=C)
+
+    gemm_launches_per_step = 1
+    hbm_peak, tc_peak, tc_sust, peak_src = load_peaks()
+
+    with ClockSampler(local_rank) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t_wall0 = time.perf_counter()
+        times = time_steps(torch, step, args.steps, args.warmup, flush, stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t_wall = time.perf_counter() - t_wall0
+    clocks = clk.summary()
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * OPS2 * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end: pinned host buffers, H2D + C ABI call + D2H every step ----
+    A_h = torch.from_numpy(d["A"]).pin_memory()
+    Bp_h = Bp.cpu().pin_memory()
+    sc_h = torch.from_numpy(d["scale"]).pin_memory()
+    C_h = torch.empty((M2, N2), dtype=torch.float16).pin_memory()
+
+    def e2e_step():
+        A.copy_(A_h, non_blocking=True)
+        Bp.copy_(Bp_h, non_blocking=True)
+        sc.copy_(sc_h, non_blocking=True)
+        bq.bq_gemm_i8xi4(A, Bp, "interleaved", col_scale=sc, out=C)
+        C_h.copy_(C, non_blocking=True)
+
+    e2e_times = time_steps(torch, e2e_step, args.steps, args.warmup, flush, stream)
+    e2e_total = sum(e2e_times)
+    if world > 1:
+        t = torch.tensor([e2e_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e = {"value": world * OPS2 * args.steps / (e2e_total * 1e-3) / 1e12, "unit": "TOPS",
+           "h2d_bytes_per_step": A_h.numel() + Bp_h.numel() + 2 * sc_h.numel(),
+           "d2h_bytes_per_step": 2 * C_h.numel(), "ms_per_step": e2e_total / args.steps}
+    del A_h, Bp_h, C_h
+
+    # ---- the M = 1 GEMV (a memory-bound kernel) ----
+    d3 = W.cfg3(M=1)
+    S = torch.from_numpy(d3["S"]).to(dev)
+    _, s3 = bq.bq_quantize_sym(S, 4)                 # per-channel scale = absmax / 7 of the source matrix
+    del S
+    X3 = torch.from_numpy(d3["X"]).to(dev)
+    W3 = bq.bq_pack_weights(torch.from_numpy(d3["W"]).to(dev), 4, "interleaved")
+    Y3 = torch.empty((1, 11008), dtype=torch.float16, device=dev)
+    gemv_times = time_steps(torch, lambda: bq.bq_gemm_f16xi4(X3, W3, s3, "interleaved", out=Y3),
+                            args.steps, args.warmup, flush, stream)
+    gemv_bytes = roofline.matmul_min_bytes(1, 4096, 11008, 16, 4, 16, extra_bytes=2 * 11008)
+    gemv_ms = statistics.median(gemv_times)
+    gemv = {"value": gemv_bytes / (gemv_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": gemv_ms, "workload": GEMV_WORKLOAD,
+            "roofline": {"bound": "hbm", "achieved": gemv_bytes / (gemv_ms * 1e-3) / 1e9, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": gemv_bytes / (gemv_ms * 1e-3) / 1e9 / hbm_peak,
+                         "peak_source": f"{peak_src} hbm_gbs"}}
+    del X3, W3, Y3
+
+    paths = {} if args.no_paths else measure_paths(torch, bq, W, roofline, dev, flush, stream, hbm_peak, tc_peak)
+    achieved = OPS2 / (statistics.mean(times) * 1e-3) / 1e12
+    traffic = ncu_traffic("gemm_tc_kernel")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "flushed between steps (512 MiB write, outside the timed events)",
+                   "mma": "tcgen05.mma kind::f16 (int8/int4 converted exactly to fp16), fp32 accumulation",
+                   "per_gpu": "independent replica of the workload on every rank"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tc_peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops (burst; fp16 dense rate equals bf16)",
+                     "kernel": "gemm_tc_kernel"},
+        "e2e": e2e, "gpu_launches": gemm_launches_per_step * args.steps, "clocks": clocks,
+        "wall_s_timed_region": t_wall, "gemv": gemv, "paths": paths,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(d, Bp.cpu().numpy())
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_paths(torch, bq, W, roofline, dev, flush, stream, hbm_peak, tc_peak, steps=10, warmup=3):
+    """The other workloads, each timed with the same protocol (median ms)."""
+    out = {}
+
+    def med(fn):
+        return statistics.median(time_steps(torch, fn, steps, warmup, flush, stream))
+
+    # quantise + INT8 x INT8, 1024 x 4096 x 4096
+    d1 = W.cfg1()
+    Wt, Xt = torch.from_numpy(d1["W"]).to(dev), torch.from_numpy(d1["X"]).to(dev)
+    wq = torch.empty((4096, 4096), dtype=torch.int8, device=dev)
+    sw = torch.empty((4096,), dtype=torch.float16, device=dev)
+    ms = med(lambda: bq.bq_quantize_sym(Wt, 8, q=wq, scale=sw))
+    qb = roofline.quantize_bytes(4096, 4096)
+    out["quantize_w_4096x4096"] = {"ms": ms, "GB/s": qb / (ms * 1e-3) / 1e9, "hbm_frac": qb / (ms * 1e-3) / 1e9 / hbm_peak}
+    xq, sx = bq.bq_quantize_sym(Xt, 8)
+    ms = med(lambda: bq.bq_gemm_i8xi8(xq, wq, row_scale=sx, col_scale=sw))
+    ops = roofline.matmul_ops(1024, 4096, 4096)
+    out["i8xi8_rowcol_1024x4096x4096"] = {"ms": ms, "TOPS": ops / (ms * 1e-3) / 1e12,
+                                          "tc_frac": ops / (ms * 1e-3) / 1e12 / tc_peak}
+    del Wt, Xt, wq, sw, xq, sx
+    # INT8 x INT4 256^3 int32
+    d0 = W.cfg0()
+    A0 = torch.from_numpy(d0["A"]).to(dev)
+    B0 = bq.bq_pack_weights(torch.from_numpy(d0["B"]).to(dev), 4, "plain")
+    ms = med(lambda: bq.bq_gemm_i8xi4(A0, B0, "plain"))
+    out["i8xi4_i32_256^3"] = {"ms": ms, "TOPS": roofline.matmul_ops(256, 256, 256) / (ms * 1e-3) / 1e12}
+    # fp16 x INT4, dynamic M
+    d3 = W.cfg3(M=1024, source=False)
+    W3 = bq.bq_pack_weights(torch.from_numpy(d3["W"]).to(dev), 4, "interleaved")
+    s3 = torch.full((11008,), 0.01, dtype=torch.float16, device=dev)
+    X3 = torch.from_numpy(d3["X"]).to(dev)
+    for M in (1, 4, 16, 64, 256, 1024):
+        Xm = X3[:M].contiguous()
+        ms = med(lambda: bq.bq_gemm_f16xi4(Xm, W3, s3, "interleaved"))
+        b = roofline.matmul_min_bytes(M, 4096, 11008, 16, 4, 16, extra_bytes=2 * 11008)
+        f = roofline.matmul_ops(M, 4096, 11008)
+        out[f"f16xi4_M{M}"] = {"ms": ms, "GB/s": b / (ms * 1e-3) / 1e9, "TFLOPS": f / (ms * 1e-3) / 1e12,
+                               "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "tc_frac": f / (ms * 1e-3) / 1e12 / tc_peak}
+    del W3, X3
+    # INT8 x ternary, N = K = 8192
+    d4 = W.cfg4(M=1024)
+    B4 = bq.bq_pack_weights(torch.from_numpy(d4["B"]).to(dev), 2, "interleaved")
+    s4 = torch.from_numpy(d4["scale"]).to(dev)
+    A4 = torch.from_numpy(d4["A"]).to(dev)
+    for M in (1, 128, 1024):
+        Am = A4[:M].contiguous()
+        ms = med(lambda: bq.bq_gemm_i8xi2(Am, B4, "interleaved", col_scale=s4))
+        b = roofline.matmul_min_bytes(M, 8192, 8192, 8, 2, 16, extra_bytes=2 * 8192)
+        f = roofline.matmul_ops(M, 8192, 8192)
+        out[f"i8xi2_M{M}"] = {"ms": ms, "GB/s": b / (ms * 1e-3) / 1e9, "TOPS": f / (ms * 1e-3) / 1e12,
+                              "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "tc_frac": f / (ms * 1e-3) / 1e12 / tc_peak}
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rows(O, a_rows, bp, scale):
+    """The oracle's whole path for a block of A rows: unpack the packed
+    weights, exact int32 GEMM, fp32 dequantisation to fp16."""
+    b = O.unpack_interleaved(bp, K2, 4)
+    return O.dequant(O.gemm_int(a_rows, b), scale)
+
+
+def cpu_baseline(d, bp, budget_s=10.0, rows=512):
+    from oracle import bq_oracle as O
+    done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and done < M2:
+        oracle_rows(O, d["A"][done:done + rows], bp, d["scale"])
+        done += rows
+    el = time.perf_counter() - t0
+    return {"value": 2 * done * N2 * K2 / el / 1e12, "unit": "TOPS", "cores": cores_used(), "kind": "oracle",
+            "sample": f"{done} of {M2} rows of A ({rows}-row blocks, each unpacking B and running the exact "
+                      f"float64-BLAS int32 GEMM + fp32 dequant), {el:.1f} s; numpy BLAS threads = all available cores"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from oracle import bq_oracle as O
+    from quantized_mixed_precision_gb300 import workloads as W
+    d = W.cfg2()
+    bp = O.pack_interleaved(d["B"], 4)
+    rows = 256
+    for i in range(args.warmup):
+        oracle_rows(O, d["A"][:rows], bp, d["scale"])
+    times = []
+    for i in range(args.steps):
+        r0 = (i * rows) % M2
+        t0 = time.perf_counter()
+        oracle_rows(O, d["A"][r0:r0 + rows], bp, d["scale"])
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = 2 * rows * N2 * K2 * args.steps / total / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": f"{rows} rows of A per step (full B, K)"},
+            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores_used(), "kind": "oracle",
+                             "sample": f"{rows} of {M2} rows of A per step"},
+            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

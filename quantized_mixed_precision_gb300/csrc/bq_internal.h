@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/bq.h"
+#include "bq.h"
 
 namespace bq {
 

@@ -392,7 +392,13 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream) {
   }
   if (g.act == ACT_I8 && g.bbits == 4) return launch_layout<ACT_I8, 4, 256, 1>(g, stream);
   if (g.act == ACT_I8 && g.bbits == 2) return launch_layout<ACT_I8, 2, 256, 1>(g, stream);
-  if (g.act == ACT_F16 && g.bbits == 4) return launch_layout<ACT_F16, 4, 256, 1>(g, stream);
+  // fp16 activations: the accumulator is not an exact integer, so K is split
+  // into two separately accumulated halves (shorter fp32 accumulation chains
+  // in the tensor core), summed in fp32 in the epilogue.
+  if (g.act == ACT_F16 && g.bbits == 4) {
+    if (nkb >= 2) return launch_layout<ACT_F16, 4, 256, 2>(g, stream);
+    return launch_layout<ACT_F16, 4, 256, 1>(g, stream);
+  }
   return cudaErrorInvalidValue;
 }
 
