@@ -42,6 +42,8 @@ struct GemmArgs {
 };
 
 // Skinny-M path (M <= 16): one pass over the weights, legacy mma.sync fp16.
+// gemv_fits tells whether its staged activations fit in shared memory.
+bool gemv_fits(int64_t M, int64_t K, int bbits);
 cudaError_t launch_gemv_mma(const GemmArgs& g, cudaStream_t stream);
 // int8 x int8 with exact int32 dp4a accumulation (any M).
 cudaError_t launch_gemm_dp4a(const GemmArgs& g, cudaStream_t stream);

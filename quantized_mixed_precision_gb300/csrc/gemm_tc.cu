@@ -352,6 +352,288 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Variant with the int8 activations in tensor memory ("TA").  Converting A
+// into shared memory costs a store and an MMA read of every A element; here
+// 4 warps (one thread per tile row, which is exactly the TMEM lane that row
+// occupies) convert their row's 64 codes of a k-block to 32 fp16 pairs and
+// write them with tcgen05.st into a TMEM stage; the MMA reads A from TMEM
+// (the [a_tmem] operand form) and only B passes through shared memory.
+//   warps 0-3   A converters (TMEM writers)
+//   warps 4-11  B converters (swizzled shared-memory tiles), then the epilogue
+//   warp 12     tensor-memory allocation and the MMA issuer (lane 0)
+// ---------------------------------------------------------------------------
+constexpr int TA_A_WARPS = 4;
+constexpr int TA_B_WARPS = 8;
+constexpr int TA_B_THREADS = TA_B_WARPS * 32;
+constexpr int TA_THREADS = (TA_A_WARPS + TA_B_WARPS + 1) * 32;
+
+template <int BBITS, int BN, int STAGES>
+struct TaCfg {
+  static constexpr int B_ROW_BYTES = BK * BBITS / 8;
+  static constexpr int B_PIECES_ROW = B_ROW_BYTES / 16;
+  static constexpr int B_PIECES = BN * B_PIECES_ROW;
+  static constexpr int NPB = (B_PIECES + TA_B_THREADS - 1) / TA_B_THREADS;
+  static constexpr int B_TILE = BN * 128;
+  static constexpr int A_COLS = BK / 2;                    // TMEM columns per A stage
+  static constexpr int NCOLS = 512;
+  static constexpr int PF = 4;
+  static constexpr size_t SMEM = (size_t)STAGES * B_TILE + 1024 + 256;
+  static_assert(BN + STAGES * A_COLS <= NCOLS, "TMEM budget");
+};
+
+template <int BBITS, int BN, bool INTER, int STAGES>
+__global__ void __launch_bounds__(TA_THREADS, 1)
+    gemm_tc_ta_kernel(const int8_t* __restrict__ a_ptr, const uint8_t* __restrict__ b_ptr, int M, int N, int K,
+                      const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
+                      void* __restrict__ out, uint64_t timeout_ns, int* status) {
+  using C = TaCfg<BBITS, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::B_TILE);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* accum_bar = empty_bar + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int m0 = blockIdx.y * BM;
+  const int n0 = blockIdx.x * BN;
+  const int nkb = K / BK;
+  constexpr int MMA_WARP = TA_A_WARPS + TA_B_WARPS;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], TA_A_WARPS * 32 + TA_B_THREADS);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(accum_bar, 1);
+    mbar_fence_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(tmem_slot, C::NCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < TA_A_WARPS) {
+    // ------------------------------------------------------------ A -> TMEM
+    const int row = m0 + warp * 32 + lane;
+    const bool row_ok = row < M;
+    const uint4* arow = reinterpret_cast<const uint4*>(a_ptr + (size_t)(row_ok ? row : 0) * K);
+    uint4 ra[C::PF][4];
+    auto load_a = [&](int kb, uint4 (&v)[4]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = row_ok ? __ldg(arow + kb * 4 + j) : make_uint4(0, 0, 0, 0);
+    };
+#pragma unroll
+    for (int p = 0; p < C::PF; ++p)
+      if (p < nkb) load_a(p, ra[p]);
+    bool ok = true;
+    for (int kb0 = 0; kb0 < nkb && ok; kb0 += C::PF) {
+#pragma unroll
+      for (int p = 0; p < C::PF; ++p) {
+        const int kb = kb0 + p;
+        if (kb < nkb && ok) {
+          uint32_t h[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            cvt_i8x4_f16(ra[p][j].x, h[8 * j + 0], h[8 * j + 1]);
+            cvt_i8x4_f16(ra[p][j].y, h[8 * j + 2], h[8 * j + 3]);
+            cvt_i8x4_f16(ra[p][j].z, h[8 * j + 4], h[8 * j + 5]);
+            cvt_i8x4_f16(ra[p][j].w, h[8 * j + 6], h[8 * j + 7]);
+          }
+          if (kb + C::PF < nkb) load_a(kb + C::PF, ra[p]);
+          const int s = kb % STAGES;
+          const bool w_ok = mbar_wait(&empty_bar[s], ((kb / STAGES) & 1) ^ 1, timeout_ns, status);
+          if (!__all_sync(0xffffffffu, w_ok)) {
+            ok = false;
+          } else {
+            tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(BN + s * C::A_COLS), h);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&full_bar[s]);
+          }
+        }
+      }
+    }
+  } else if (warp < MMA_WARP) {
+    // ------------------------------------------------------------ B -> smem
+    const int c = tid - TA_A_WARPS * 32;
+    const size_t b_row_stride = (size_t)K * BBITS / 8;
+    uint4 rb[C::PF][C::NPB];
+    auto load_b = [&](int kb, uint4 (&v)[C::NPB]) {
+#pragma unroll
+      for (int i = 0; i < C::NPB; ++i) {
+        const int pi = c + i * TA_B_THREADS;
+        const int r = pi / C::B_PIECES_ROW, sub = pi % C::B_PIECES_ROW;
+        v[i] = (pi < C::B_PIECES && n0 + r < N)
+                   ? __ldg(reinterpret_cast<const uint4*>(b_ptr + (size_t)(n0 + r) * b_row_stride +
+                                                          (size_t)kb * C::B_ROW_BYTES + sub * 16))
+                   : make_uint4(0, 0, 0, 0);
+      }
+    };
+    auto store_b = [&](uint8_t* tb, const uint4 (&v)[C::NPB]) {
+#pragma unroll
+      for (int i = 0; i < C::NPB; ++i) {
+        const int pi = c + i * TA_B_THREADS;
+        if (pi >= C::B_PIECES) continue;
+        const int r = pi / C::B_PIECES_ROW, sub = pi % C::B_PIECES_ROW;
+        const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        if constexpr (BBITS == 8) {
+          uint4 o0, o1;
+          cvt_i8x4_f16(wv[0], o0.x, o0.y);
+          cvt_i8x4_f16(wv[1], o0.z, o0.w);
+          cvt_i8x4_f16(wv[2], o1.x, o1.y);
+          cvt_i8x4_f16(wv[3], o1.z, o1.w);
+          st_chunk(tb, r, 2 * sub, o0);
+          st_chunk(tb, r, 2 * sub + 1, o1);
+        } else if constexpr (BBITS == 4) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t h[4];
+            cvt_i4x8_f16(INTER ? wv[j] : plain_to_inter_i4(wv[j]), h);
+            st_chunk(tb, r, 4 * sub + j, make_uint4(h[0], h[1], h[2], h[3]));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t h[8];
+            cvt_i2x16_f16(INTER ? wv[j] : plain_to_inter_i2(wv[j]), h);
+            st_chunk(tb, r, 8 * sub + 2 * j, make_uint4(h[0], h[1], h[2], h[3]));
+            st_chunk(tb, r, 8 * sub + 2 * j + 1, make_uint4(h[4], h[5], h[6], h[7]));
+          }
+        }
+      }
+    };
+#pragma unroll
+    for (int p = 0; p < C::PF; ++p)
+      if (p < nkb) load_b(p, rb[p]);
+    bool ok = true;
+    for (int kb0 = 0; kb0 < nkb && ok; kb0 += C::PF) {
+#pragma unroll
+      for (int p = 0; p < C::PF; ++p) {
+        const int kb = kb0 + p;
+        if (kb < nkb && ok) {
+          const int s = kb % STAGES;
+          const bool w_ok = mbar_wait(&empty_bar[s], ((kb / STAGES) & 1) ^ 1, timeout_ns, status);
+          if (!__all_sync(0xffffffffu, w_ok)) {
+            ok = false;
+          } else {
+            store_b(smem + s * C::B_TILE, rb[p]);
+            fence_proxy_async_smem();
+            mbar_arrive(&full_bar[s]);
+            if (kb + C::PF < nkb) load_b(kb + C::PF, rb[p]);
+          }
+        }
+      }
+    }
+
+    // ------------------------------------------------------------ epilogue
+    const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(accum_bar, 0, ok ? timeout_ns : 0, status));
+    tc_fence_after();
+    if (acc_ok) {
+      const int q = warp & 3;                       // TMEM lane quadrant of this warp
+      const int chalf = (warp - TA_A_WARPS) >> 2;   // column half
+      const int row = m0 + 32 * q + lane;
+      const bool row_ok = row < M;
+      float rsc = 1.0f;
+      if (epi == EPI_F16_ROWCOL && row_ok) rsc = __half2float(row_scale[row]);
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 64; ++cc) {
+        const int col = chalf * (BN / 2) + cc * 32;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
+        tmem_ld_wait();
+        const int ncol = n0 + col;
+        if (row_ok && ncol < N) {
+          if (epi == EPI_I32) {
+            int4* dst = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + (size_t)row * N + ncol);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_int4(__float2int_rn(__uint_as_float(r[4 * i])), __float2int_rn(__uint_as_float(r[4 * i + 1])),
+                                 __float2int_rn(__uint_as_float(r[4 * i + 2])),
+                                 __float2int_rn(__uint_as_float(r[4 * i + 3])));
+          } else {
+            uint32_t hv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float x0 = __fmul_rn(__uint_as_float(r[2 * i]), __half2float(col_scale[ncol + 2 * i]));
+              float x1 = __fmul_rn(__uint_as_float(r[2 * i + 1]), __half2float(col_scale[ncol + 2 * i + 1]));
+              if (epi == EPI_F16_ROWCOL) {
+                x0 = __fmul_rn(x0, rsc);
+                x1 = __fmul_rn(x1, rsc);
+              }
+              const __half2 h2 = __halves2half2(__float2half_rn(x0), __float2half_rn(x1));
+              hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(out) + (size_t)row * N + ncol);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(BM, BN);
+      const uint32_t smem_base = smem_u32(smem);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % STAGES;
+        if (!mbar_wait(&full_bar[s], (kb / STAGES) & 1, timeout_ns, status)) break;
+        tc_fence_after();
+        const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::B_TILE);
+        const uint32_t a_tm = tmem + (uint32_t)(BN + s * C::A_COLS);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          // 16 k = 8 TMEM columns of A; 32 bytes along K in the swizzled B tile
+          tc_mma_f16_ts(tmem, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (kb == 0 && kk == 0) ? 0u : 1u);
+        }
+        tc_commit(&empty_bar[s]);
+      }
+      tc_commit(accum_bar);
+      mbar_wait(accum_bar, 0, DRAIN_TIMEOUT_NS, status);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::NCOLS);
+  }
+}
+
+template <int BBITS, int BN, bool INTER>
+cudaError_t launch_ta(const GemmArgs& g, cudaStream_t stream) {
+  constexpr int STAGES = 4;
+  using C = TaCfg<BBITS, BN, STAGES>;
+  int* status = nullptr;
+  cudaError_t se = device_status_ptr(&status);
+  if (se != cudaSuccess) return se;
+  auto kern = gemm_tc_ta_kernel<BBITS, BN, INTER, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
+  kern<<<grid, TA_THREADS, C::SMEM, stream>>>(static_cast<const int8_t*>(g.a), static_cast<const uint8_t*>(g.b),
+                                              (int)g.M, (int)g.N, (int)g.K,
+                                              reinterpret_cast<const __half*>(g.row_scale),
+                                              reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c,
+                                              (uint64_t)wait_timeout_ns(), status);
+  return cudaGetLastError();
+}
+
+template <int BBITS, int BN>
+cudaError_t launch_ta_layout(const GemmArgs& g, cudaStream_t stream) {
+  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_ta<BBITS, BN, false>(g, stream);
+  return launch_ta<BBITS, BN, true>(g, stream);
+}
+
 template <int ACT, int BBITS, int BN, int NACC, bool INTER>
 cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
   constexpr int STAGES = 4;
@@ -388,10 +670,11 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream) {
       if (nkb <= 64) return launch_layout<ACT_I8, 8, 128, 4>(g, stream);
       return cudaErrorInvalidValue;
     }
-    return launch_layout<ACT_I8, 8, 256, 1>(g, stream);
+    return launch_ta_layout<8, 256>(g, stream);
   }
-  if (g.act == ACT_I8 && g.bbits == 4) return launch_layout<ACT_I8, 4, 256, 1>(g, stream);
-  if (g.act == ACT_I8 && g.bbits == 2) return launch_layout<ACT_I8, 2, 256, 1>(g, stream);
+  // int8 activations with 4- / 2-bit weights: every partial sum < 2**24 (host-bounded K)
+  if (g.act == ACT_I8 && g.bbits == 4) return launch_ta_layout<4, 256>(g, stream);
+  if (g.act == ACT_I8 && g.bbits == 2) return launch_ta_layout<2, 256>(g, stream);
   // fp16 activations: the accumulator is not an exact integer, so K is split
   // into two separately accumulated halves (shorter fp32 accumulation chains
   // in the tensor core), summed in fp32 in the epilogue.

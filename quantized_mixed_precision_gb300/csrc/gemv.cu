@@ -3,14 +3,14 @@
 // The work is bound by reading the weights from HBM once (the decode-step
 // use of the quantised linear in "BMINF的後訓練量化實現", 實現代碼分析2, runs
 // with M = batch).  A block of 4 warps owns 16 weight rows; each warp takes a
-// quarter of K.  Every thread issues all of its 16-byte weight loads (two
-// rows, up to UNITS steps) before consuming any, so a warp keeps ~8 KB in
-// flight; the codes are turned into fp16 pairs in registers (exact) and fed
-// straight into mma.sync m16n8k16 as the A fragment, so weights never touch
-// shared memory.  The activations (at most 16 rows, L1/L2 resident) are read
-// from global memory as B fragments; int8 activations are converted to fp16
-// exactly on the way.  Accumulation is fp32; for integer operands every
-// partial sum stays below 2**24 (bounded on the host), so it is exact.
+// quarter of K.  Every thread first issues all of its 16-byte weight loads
+// (two rows, up to UNITS steps: ~8 KB per warp in flight); while they are in
+// flight the block stages the activations (at most 16 rows, as fp16; int8
+// activations are converted exactly on the way) into shared memory.  The
+// codes are then turned into fp16 pairs in registers (exact) and fed straight
+// into mma.sync m16n8k16 as the A fragment, so weights never touch shared
+// memory.  Accumulation is fp32; for integer operands every partial sum stays
+// below 2**24 (bounded on the host), so it is exact.
 //
 // K-permutation: inside one MMA the hardware pairs A column k with B row k.
 // Thread t of a quad loads weight bytes [16t, 16t + 16) of a step; its fp16
@@ -35,7 +35,20 @@ struct GemvCfg {
   static constexpr int STEP = 4 * E16;                // k per step (4 threads of a quad)
   static constexpr int PW = 16 / BBITS;               // fp16 pairs per 32-bit word
   static constexpr int KW = 32 / BBITS;               // k per 32-bit word
+  static constexpr int PAD = BBITS == 4 ? 16 : 64;    // staged activation row pad (bytes)
+  // Chunk position inside a staged activation row.  Thread t of a quad reads
+  // chunks [t * E16 / 8, (t + 1) * E16 / 8) of a step; with this swizzle and
+  // the row pad the 8 threads of a quarter warp (2 rows x 4 quads) hit 8
+  // different 16-byte bank groups.
+  __device__ __forceinline__ static int swz(int c) {
+    return BBITS == 4 ? (c ^ (((c >> 3) & 1) << 1)) : (c ^ ((c >> 3) & 7));
+  }
 };
+
+template <int BBITS>
+constexpr int gemv_smem_bytes(int M, int K) {
+  return M * (2 * K + GemvCfg<BBITS>::PAD);
+}
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
@@ -55,20 +68,6 @@ __device__ __forceinline__ void convert_word(uint32_t w, uint32_t (&h)[GemvCfg<B
   }
 }
 
-// 8 activation values (k0 .. k0+7) of row m as 4 fp16x2 words.
-template <int ACT>
-__device__ __forceinline__ uint4 load_x8(const void* act, int m, int K, int k0) {
-  if constexpr (ACT == ACT_F16) {
-    return __ldg(reinterpret_cast<const uint4*>(static_cast<const __half*>(act) + (size_t)m * K + k0));
-  } else {
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const int8_t*>(act) + (size_t)m * K + k0));
-    uint4 v;
-    cvt_i8x4_f16(raw.x, v.x, v.y);
-    cvt_i8x4_f16(raw.y, v.z, v.w);
-    return v;
-  }
-}
-
 template <int BBITS, int ACT, int NB, bool INTER>
 __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void* __restrict__ act,
                                                                       const uint8_t* __restrict__ w, int M, int N,
@@ -77,6 +76,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
                                                                       void* __restrict__ out) {
   using C = GemvCfg<BBITS>;
   __shared__ float red[GEMV_WARPS][NB][4][32];
+  extern __shared__ __align__(16) uint8_t xs[];       // M staged activation rows
+  const int rs = 2 * K + C::PAD;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -94,7 +95,9 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
 #pragma unroll
     for (int i = 0; i < 4; ++i) d[nb][i] = 0.0f;
 
-  for (int s0 = s_begin; s0 < s_end; s0 += UNITS) {
+  // The first iteration always runs (every warp takes part in the staging
+  // barrier, even one with no steps of its own).
+  for (int s0 = s_begin, first = 1; s0 < s_end || first; s0 += UNITS, first = 0) {
     uint4 v0[UNITS], v1[UNITS];
 #pragma unroll
     for (int u = 0; u < UNITS; ++u) {
@@ -108,6 +111,24 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
         v0[u] = make_uint4(0, 0, 0, 0);
         v1[u] = make_uint4(0, 0, 0, 0);
       }
+    }
+    if (first) {
+      // stage the activations while the first weight loads are in flight
+      const int chunks_per_row = K >> 3;
+      for (int idx = threadIdx.x; idx < M * chunks_per_row; idx += blockDim.x) {
+        const int m = idx / chunks_per_row, c = idx - m * chunks_per_row;
+        uint4 v;
+        if constexpr (ACT == ACT_F16) {
+          v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __half*>(act) + (size_t)m * K) + c);
+        } else {
+          const uint2 raw =
+              __ldg(reinterpret_cast<const uint2*>(static_cast<const int8_t*>(act) + (size_t)m * K) + c);
+          cvt_i8x4_f16(raw.x, v.x, v.y);
+          cvt_i8x4_f16(raw.y, v.z, v.w);
+        }
+        *reinterpret_cast<uint4*>(xs + (size_t)m * rs + C::swz(c) * 16) = v;
+      }
+      __syncthreads();
     }
 #pragma unroll
     for (int u = 0; u < UNITS; ++u) {
@@ -126,12 +147,13 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
         convert_word<BBITS, INTER>(wb[i], hb);
 #pragma unroll
         for (int c = 0; c < C::PW / 4; ++c) {
-          const int k0 = kbase + i * C::KW + 8 * c;
+          const int chunk = (kbase >> 3) + i * (C::KW / 8) + c;
           uint4 xb[NB];
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
             const int m = nb * 8 + g;
-            xb[nb] = (m < M && kin) ? load_x8<ACT>(act, m, K, k0) : make_uint4(0, 0, 0, 0);
+            xb[nb] = (m < M && kin) ? *reinterpret_cast<const uint4*>(xs + (size_t)m * rs + C::swz(chunk) * 16)
+                                    : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
@@ -173,7 +195,13 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
 
 template <int BBITS, int ACT, int NB, bool INTER>
 cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
-  gemv_mma_kernel<BBITS, ACT, NB, INTER><<<(unsigned)(g.N / 16), GEMV_WARPS * 32, 0, stream>>>(
+  const int smem = gemv_smem_bytes<BBITS>((int)g.M, (int)g.K);
+  auto kern = gemv_mma_kernel<BBITS, ACT, NB, INTER>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)(g.N / 16), GEMV_WARPS * 32, smem, stream>>>(
       g.a, static_cast<const uint8_t*>(g.b), (int)g.M, (int)g.N, (int)g.K,
       reinterpret_cast<const __half*>(g.row_scale), reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c);
   return cudaGetLastError();
@@ -188,8 +216,13 @@ cudaError_t launch_bits_act(const GemmArgs& g, cudaStream_t stream) {
 
 }  // namespace
 
+bool gemv_fits(int64_t M, int64_t K, int bbits) {
+  const int64_t bytes = M * (2 * K + (bbits == 4 ? 16 : 64));
+  return M >= 1 && M <= 16 && bytes <= 200 * 1024;
+}
+
 cudaError_t launch_gemv_mma(const GemmArgs& g, cudaStream_t stream) {
-  if (g.M < 1 || g.M > 16) return cudaErrorInvalidValue;
+  if (!gemv_fits(g.M, g.K, g.bbits)) return cudaErrorInvalidValue;
   if (g.bbits == 4) {
     return g.act == ACT_F16 ? launch_bits_act<4, ACT_F16>(g, stream) : launch_bits_act<4, ACT_I8>(g, stream);
   }

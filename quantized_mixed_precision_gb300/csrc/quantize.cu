@@ -5,7 +5,7 @@
 // abs(row absmax) / D stored as fp16, and the codes are nearbyint(x / scale)
 // computed from that stored scale (quantize_copy_float), or with the quotient
 // first rounded to fp16 (quantize_copy_half).  The page runs a reduction
-// kernel and then an elementwise kernel, reading x twice; here one warp keeps
+// kernel and then an elementwise kernel, reading x twice; here one block keeps
 // its row in registers so x is read from HBM once.
 #include <cuda_fp16.h>
 
@@ -18,11 +18,21 @@ namespace {
 
 __device__ __forceinline__ int qmax_of(int bits) { return bits == 8 ? 127 : (bits == 4 ? 7 : 1); }
 
-// Code for one element from the stored fp16 scale (as float).
-__device__ __forceinline__ int quant_one(float x, float s, int d, int mode) {
+// Code for one element from the stored fp16 scale s (as float) and its
+// reciprocal rcp = RN(1 / s).  In F32DIV mode the code is rne(RN(x / s)).
+// RN(x * rcp) differs from RN(x / s) by less than 2**-14 for |x / s| < 256,
+// so the two round to the same integer unless the product lies within 2**-12
+// of a half-integer; only then is the IEEE division evaluated.
+__device__ __forceinline__ int quant_one(float x, float s, float rcp, int d, int mode) {
   if (s == 0.0f) return 0;
-  float t = __fdiv_rn(x, s);
-  if (mode == BQ_ROUND_BMINF_HALF) t = __half2float(__float2half_rn(t));
+  float t;
+  if (mode == BQ_ROUND_BMINF_HALF) {
+    t = __half2float(__float2half_rn(__fdiv_rn(x, s)));
+  } else {
+    t = __fmul_rn(x, rcp);
+    const float frac = t - floorf(t);
+    if (fabsf(frac - 0.5f) < 2.44140625e-4f || fabsf(t) >= 256.0f) t = __fdiv_rn(x, s);
+  }
   int r = __float2int_rn(t);  // round to nearest, ties to even
   return r > d ? d : (r < -d ? -d : r);
 }
@@ -33,31 +43,29 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// One warp per row; the row (cols fp16, cols % 8 == 0, cols <= 256 * VPL)
-// lives in registers as VPL 16-byte vectors per lane (cols <= 4096).
-template <int VPL>
-__global__ void __launch_bounds__(256) quantize_rows_f16_kernel(const __half* __restrict__ x, int64_t rows,
-                                                                int64_t cols, int64_t ld_x, int bits, int mode,
-                                                                int8_t* __restrict__ q,
-                                                                __half* __restrict__ scale) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= rows) return;
+// One 128-thread block per row; the row (fp16, cols % 8 == 0,
+// cols <= 1024 * VPT) lives in registers as VPT 16-byte vectors per thread,
+// so x is read from HBM exactly once.
+constexpr int QT = 128;
+
+template <int VPT>
+__global__ void __launch_bounds__(QT) quantize_rows_f16_kernel(const __half* __restrict__ x, int64_t rows,
+                                                               int64_t cols, int64_t ld_x, int bits, int mode,
+                                                               int8_t* __restrict__ q, __half* __restrict__ scale) {
+  __shared__ float red[QT / 32];
+  const int tid = threadIdx.x;
+  const int64_t row = blockIdx.x;
   const int nvec = (int)(cols >> 3);
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * ld_x);
-  uint4 v[VPL];
+  uint4 v[VPT];
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int idx = lane + 32 * i;
-    if (idx < nvec) {
-      v[i] = __ldcs(xr + idx);  // streamed once
-    } else {
-      v[i] = make_uint4(0, 0, 0, 0);
-    }
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = tid + QT * i;
+    v[i] = idx < nvec ? __ldcs(xr + idx) : make_uint4(0, 0, 0, 0);   // streamed once
   }
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) {
+  for (int i = 0; i < VPT; ++i) {
     const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -66,14 +74,19 @@ __global__ void __launch_bounds__(256) quantize_rows_f16_kernel(const __half* __
     }
   }
   amax = warp_max(amax);
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < QT / 32; ++w) amax = fmaxf(amax, red[w]);
   const int d = qmax_of(bits);
   const __half sh = __float2half_rn(__fdiv_rn(amax, (float)d));
   const float s = __half2float(sh);
-  if (lane == 0) scale[row] = sh;
+  const float rcp = s == 0.0f ? 0.0f : __frcp_rn(s);
+  if (tid == 0) scale[row] = sh;
   uint2* qr = reinterpret_cast<uint2*>(q + row * cols);
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int idx = lane + 32 * i;
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = tid + QT * i;
     if (idx < nvec) {
       const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
       uint32_t packed[2];
@@ -81,10 +94,10 @@ __global__ void __launch_bounds__(256) quantize_rows_f16_kernel(const __half* __
       for (int j = 0; j < 2; ++j) {
         const float2 f0 = __half22float2(h[2 * j]);
         const float2 f1 = __half22float2(h[2 * j + 1]);
-        const uint32_t b0 = (uint32_t)(quant_one(f0.x, s, d, mode) & 0xff);
-        const uint32_t b1 = (uint32_t)(quant_one(f0.y, s, d, mode) & 0xff);
-        const uint32_t b2 = (uint32_t)(quant_one(f1.x, s, d, mode) & 0xff);
-        const uint32_t b3 = (uint32_t)(quant_one(f1.y, s, d, mode) & 0xff);
+        const uint32_t b0 = (uint32_t)(quant_one(f0.x, s, rcp, d, mode) & 0xff);
+        const uint32_t b1 = (uint32_t)(quant_one(f0.y, s, rcp, d, mode) & 0xff);
+        const uint32_t b2 = (uint32_t)(quant_one(f1.x, s, rcp, d, mode) & 0xff);
+        const uint32_t b3 = (uint32_t)(quant_one(f1.y, s, rcp, d, mode) & 0xff);
         packed[j] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
       }
       __stcs(qr + idx, make_uint2(packed[0], packed[1]));
@@ -129,17 +142,17 @@ __global__ void __launch_bounds__(256) quantize_rows_generic_kernel(const T* __r
   const int d = qmax_of(bits);
   const __half sh = __float2half_rn(__fdiv_rn(amax, (float)d));
   const float s = __half2float(sh);
+  const float rcp = s == 0.0f ? 0.0f : __frcp_rn(s);
   if (threadIdx.x == 0) scale[row] = sh;
   int8_t* qr = q + row * cols;
-  for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) qr[c] = (int8_t)quant_one(load_as_float(xr + c), s, d, mode);
+  for (int64_t c = threadIdx.x; c < cols; c += blockDim.x)
+    qr[c] = (int8_t)quant_one(load_as_float(xr + c), s, rcp, d, mode);
 }
 
-template <int VPL>
+template <int VPT>
 cudaError_t launch_rows_f16(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int bits, int mode, int8_t* q,
                             uint16_t* scale, cudaStream_t stream) {
-  const int warps = 8;
-  const int64_t blocks = (rows + warps - 1) / warps;
-  quantize_rows_f16_kernel<VPL><<<(unsigned)blocks, warps * 32, 0, stream>>>(
+  quantize_rows_f16_kernel<VPT><<<(unsigned)rows, QT, 0, stream>>>(
       static_cast<const __half*>(x), rows, cols, ld_x, bits, mode, q, reinterpret_cast<__half*>(scale));
   return cudaGetLastError();
 }
@@ -153,15 +166,13 @@ cudaError_t launch_quantize(const void* x, int xtype, int64_t rows, int64_t cols
     // absmax of an empty row is 0: scale 0, no codes
     return cudaMemsetAsync(scale, 0, (size_t)rows * sizeof(uint16_t), stream);
   }
+  if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
   const bool vec_ok = xtype == BQ_F16 && (cols % 8) == 0 && (ld_x % 8) == 0 && cols <= 4096 &&
                       (reinterpret_cast<uintptr_t>(x) % 16) == 0 && (reinterpret_cast<uintptr_t>(q) % 8) == 0;
   if (vec_ok) {
-    const int64_t nvec = cols / 8;
-    if (nvec <= 32) return launch_rows_f16<1>(x, rows, cols, ld_x, bits, mode, q, scale, stream);
-    if (nvec <= 64) return launch_rows_f16<2>(x, rows, cols, ld_x, bits, mode, q, scale, stream);
-    if (nvec <= 128) return launch_rows_f16<4>(x, rows, cols, ld_x, bits, mode, q, scale, stream);
-    if (nvec <= 256) return launch_rows_f16<8>(x, rows, cols, ld_x, bits, mode, q, scale, stream);
-    return launch_rows_f16<16>(x, rows, cols, ld_x, bits, mode, q, scale, stream);
+    if (cols <= 1024) return launch_rows_f16<1>(x, rows, cols, ld_x, bits, mode, q, scale, stream);
+    if (cols <= 2048) return launch_rows_f16<2>(x, rows, cols, ld_x, bits, mode, q, scale, stream);
+    return launch_rows_f16<4>(x, rows, cols, ld_x, bits, mode, q, scale, stream);
   }
   if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (xtype == BQ_F16) {
