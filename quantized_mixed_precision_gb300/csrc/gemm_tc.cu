@@ -12,20 +12,31 @@
 // fp16 (int8, int4 and int2 values are fp16 integers) and multiplied with
 // tcgen05.mma kind::f16 into an fp32 accumulator in tensor memory.  Integer
 // products are exact and every partial sum is an integer; while those stay
-// below 2**24 the fp32 accumulation is exact too (the host guarantees that for
-// the int32 paths by bounding K, or by splitting K into separately
-// accumulated slices that are summed as integers in the epilogue).
+// below 2**24 the fp32 accumulation is exact too.  The host guarantees that
+// for the int32 paths by bounding K, or by splitting K into separately
+// accumulated TMEM slices of at most 1024 k that the epilogue sums as
+// integers.  fp16 activations accumulate in two slices (shorter fp32 chains).
 //
-// CTA organisation (one 128 x BN output tile per CTA):
-//   warps 0-7  converters: 16-byte global loads of the raw A / B k-blocks into
-//              registers (PF k-blocks ahead), exact conversion to fp16, stores
-//              into a STAGES-deep ring of 128-byte-swizzled K-major tiles;
-//              afterwards the epilogue (TMEM -> registers -> global).
-//   warp 8     allocates tensor memory; lane 0 issues the MMAs (4 per 64-wide
-//              k-block) and commits each stage back to the converters.
+// One 128 x BN output tile per CTA; warp roles:
+//   producer warp  one thread issues 2-D TMA loads (cp.async.bulk.tensor) of
+//                  the raw k-blocks of B (and of A) into a ring of RST raw
+//                  stages; rows past M / N arrive zero-filled.
+//   A warps (4)    int8 activations only: thread = tile row = TMEM lane; reads
+//                  its 64 raw codes (64B-swizzled, conflict-free), converts
+//                  them to 32 fp16 pairs and writes them with tcgen05.st into
+//                  a TMEM stage that the MMA reads as its A operand.
+//                  fp16 activations need no conversion: the producer loads
+//                  them with TMA straight into the 128B-swizzled MMA layout.
+//   B warps (8)    read raw weight codes, convert them to fp16 and store the
+//                  128B-swizzled K-major tile the MMA reads; after the
+//                  mainloop they run the epilogue (TMEM -> registers -> HBM).
+//   MMA warp       allocates tensor memory; lane 0 issues 4 MMAs per 64-wide
+//                  k-block and commits each stage back to its producers.
 // Every mbarrier wait is bounded in time; a wait that gives up records
-// BQ_ERR_TIMEOUT, the CTA abandons the tile, waits (bounded) for MMAs it
-// issued, frees tensor memory and exits.
+// BQ_ERR_TIMEOUT, the CTA abandons the tile, waits (bounded) for the TMA
+// loads and MMAs it issued, frees tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "bq_device.cuh"
@@ -71,53 +82,97 @@ cudaError_t read_device_status(int* status_out, bool reset) {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;               // fp16 elements per 128-byte swizzle row
-constexpr int CONV_WARPS = 8;
-constexpr int CONV_THREADS = CONV_WARPS * 32;
-constexpr int TC_THREADS = CONV_THREADS + 32;
+constexpr int BK = 64;                 // k per block: one 128-byte fp16 swizzle row
+constexpr int B_WARPS = 8;
+constexpr int B_THREADS = B_WARPS * 32;
 constexpr uint64_t DRAIN_TIMEOUT_NS = 4000000000ull;
 
-template <int ACT, int BBITS, int BN, int NACC, bool INTER, int STAGES>
-struct TcCfg {
-  static constexpr int A_ROW_BYTES = ACT == ACT_F16 ? BK * 2 : BK;      // raw bytes per A row per k-block
-  static constexpr int B_ROW_BYTES = BK * BBITS / 8;                     // raw bytes per B row per k-block
-  static constexpr int A_PIECES_ROW = A_ROW_BYTES / 16;
-  static constexpr int B_PIECES_ROW = B_ROW_BYTES / 16;
-  static constexpr int A_PIECES = BM * A_PIECES_ROW;
+enum AMode : int { A_I8_TMEM = 0, A_F16_SMEM = 1 };
+
+template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST>
+struct Cfg {
+  static constexpr int A_WARPS = AMODE == A_I8_TMEM ? 4 : 0;
+  static constexpr int MMA_WARP = A_WARPS + B_WARPS;
+  static constexpr int PRODUCER_WARP = MMA_WARP + 1;
+  static constexpr int THREADS = (PRODUCER_WARP + 1) * 32;
+  static constexpr int B_RAW_ROW = BK * BBITS / 8;            // raw weight bytes per row per k-block
+  static constexpr int B_PIECES_ROW = B_RAW_ROW / 16;
   static constexpr int B_PIECES = BN * B_PIECES_ROW;
-  static constexpr int NPA = (A_PIECES + CONV_THREADS - 1) / CONV_THREADS;
-  static constexpr int NPB = (B_PIECES + CONV_THREADS - 1) / CONV_THREADS;
-  static constexpr int A_TILE = BM * 128;                                // fp16 tile bytes
+  static constexpr int NPB = (B_PIECES + B_THREADS - 1) / B_THREADS;
+  static constexpr int B_RAW = BN * B_RAW_ROW;
+  static constexpr int A_RAW = AMODE == A_I8_TMEM ? BM * BK : 0;   // int8 raw A per k-block
+  static constexpr int A_TILE = AMODE == A_F16_SMEM ? BM * 128 : 0; // fp16 A tile in the MMA stage
   static constexpr int B_TILE = BN * 128;
-  static constexpr int STAGE_BYTES = A_TILE + B_TILE;
-  static constexpr int NCOLS = NACC * BN;                                // TMEM columns
-  static constexpr int PF = 3;                                           // register prefetch depth
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
-  static_assert(NCOLS <= 512 && (NCOLS & (NCOLS - 1)) == 0, "TMEM columns must be a power of two <= 512");
-  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+  static constexpr int STAGE = A_TILE + B_TILE;
+  static constexpr int RSTAGE = A_RAW + B_RAW;
+  static constexpr int A_COLS = BK / 2;                        // TMEM columns of one A stage
+  static constexpr int ACC_COLS = NACC * BN;
+  static constexpr int USED_COLS = ACC_COLS + (AMODE == A_I8_TMEM ? ST * A_COLS : 0);
+  static constexpr int NCOLS = USED_COLS <= 128 ? 128 : (USED_COLS <= 256 ? 256 : 512);
+  static constexpr int OFF_RAW = ST * STAGE;
+  static constexpr int OFF_BAR = OFF_RAW + RST * RSTAGE;
+  static constexpr size_t SMEM = (size_t)OFF_BAR + 256 + 1024;
+  static_assert(USED_COLS <= 512, "tensor memory budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(STAGE % 1024 == 0 && RSTAGE % 1024 == 0, "stage alignment");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
 };
 
-struct RawPiece {
-  uint4 v;
-};
-
-// Store one 16-byte fp16 chunk (logical chunk lc, 8 k values) of row r into a
-// 128B-swizzled K-major tile.
+// Store one 16-byte fp16 chunk (logical chunk lc = 8 k values) of row r into a
+// 128B-swizzled K-major tile (chunk c of row r lives at position c ^ (r & 7)).
 __device__ __forceinline__ void st_chunk(uint8_t* tile, int r, int lc, uint4 v) {
   *reinterpret_cast<uint4*>(tile + r * 128 + ((lc ^ (r & 7)) << 4)) = v;
 }
 
-template <int ACT, int BBITS, int BN, int NACC, bool INTER, int STAGES>
-__global__ void __launch_bounds__(TC_THREADS, 1)
-    gemm_tc_kernel(const void* __restrict__ a_ptr, const uint8_t* __restrict__ b_ptr, int M, int N, int K,
-                   const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
+// Convert one 16-byte raw weight piece (row r, piece sub) and store it.
+template <int BBITS, bool INTER>
+__device__ __forceinline__ void convert_b_piece(uint8_t* tb, int r, int sub, const uint4& v) {
+  const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (BBITS == 8) {
+    uint4 o0, o1;
+    cvt_i8x4_f16(wv[0], o0.x, o0.y);
+    cvt_i8x4_f16(wv[1], o0.z, o0.w);
+    cvt_i8x4_f16(wv[2], o1.x, o1.y);
+    cvt_i8x4_f16(wv[3], o1.z, o1.w);
+    st_chunk(tb, r, 2 * sub, o0);
+    st_chunk(tb, r, 2 * sub + 1, o1);
+  } else if constexpr (BBITS == 4) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t h[4];
+      cvt_i4x8_f16(INTER ? wv[j] : plain_to_inter_i4(wv[j]), h);
+      st_chunk(tb, r, 4 * sub + j, make_uint4(h[0], h[1], h[2], h[3]));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t h[8];
+      cvt_i2x16_f16(INTER ? wv[j] : plain_to_inter_i2(wv[j]), h);
+      st_chunk(tb, r, 8 * sub + 2 * j, make_uint4(h[0], h[1], h[2], h[3]));
+      st_chunk(tb, r, 8 * sub + 2 * j + 1, make_uint4(h[4], h[5], h[6], h[7]));
+    }
+  }
+}
+
+// Wait on an mbarrier phase with every lane of the warp; true only if all
+// lanes saw it complete (a warp-uniform decision).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, timeout_ns, status));
+}
+
+template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST>
+__global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST>::THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
+                   int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
                    void* __restrict__ out, uint64_t timeout_ns, int* status) {
-  using C = TcCfg<ACT, BBITS, BN, NACC, INTER, STAGES>;
+  using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
-  uint64_t* empty_bar = full_bar + STAGES;
-  uint64_t* accum_bar = empty_bar + STAGES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);   // MMA stage ready
+  uint64_t* empty_bar = full_bar + ST;                                   // MMA stage consumed
+  uint64_t* rfull_bar = empty_bar + ST;                                  // raw stage landed
+  uint64_t* rempty_bar = rfull_bar + RST;                                // raw stage read
+  uint64_t* accum_bar = rempty_bar + RST;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
 
   const int tid = threadIdx.x;
@@ -125,143 +180,162 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int m0 = blockIdx.y * BM;
   const int n0 = blockIdx.x * BN;
   const int nkb = K / BK;
+  constexpr int CONSUMERS = (C::A_WARPS + B_WARPS) * 32;
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], CONV_THREADS);
+    for (int s = 0; s < ST; ++s) {
+      // fp16 A: the producer's expect-tx arrival plus the B converters
+      mbar_init(&full_bar[s], AMODE == A_F16_SMEM ? 1 + B_THREADS : CONSUMERS);
       mbar_init(&empty_bar[s], 1);
+    }
+    for (int s = 0; s < RST; ++s) {
+      mbar_init(&rfull_bar[s], 1);
+      mbar_init(&rempty_bar[s], CONSUMERS);
     }
     mbar_init(accum_bar, 1);
     mbar_fence_init();
   }
-  if (warp == CONV_WARPS) {
+  if (warp == C::MMA_WARP) {
     tmem_alloc(tmem_slot, C::NCOLS);
     tmem_relinquish();
+  }
+  if (warp == C::PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < CONV_WARPS) {
-    // ------------------------------------------------------------------ converters
-    const int c = tid;
-    const size_t a_row_stride = (size_t)K * (ACT == ACT_F16 ? 2 : 1);
-    const size_t b_row_stride = (size_t)K * BBITS / 8;
-    const uint8_t* a_bytes = static_cast<const uint8_t*>(a_ptr);
-
-    RawPiece ra[C::PF][C::NPA], rb[C::PF][C::NPB];
-
-    auto load_kb = [&](int kb, RawPiece (&pa)[C::NPA], RawPiece (&pb)[C::NPB]) {
-#pragma unroll
-      for (int i = 0; i < C::NPA; ++i) {
-        const int pi = c + i * CONV_THREADS;
-        const int r = pi / C::A_PIECES_ROW, sub = pi % C::A_PIECES_ROW;
-        if (pi < C::A_PIECES && m0 + r < M) {
-          pa[i].v = __ldg(reinterpret_cast<const uint4*>(a_bytes + (size_t)(m0 + r) * a_row_stride +
-                                                          (size_t)kb * C::A_ROW_BYTES + sub * 16));
+  if (warp == C::PRODUCER_WARP) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int rs = kb % RST;
+        if (!mbar_wait(&rempty_bar[rs], ((kb / RST) & 1) ^ 1, timeout_ns, status)) break;
+        uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE;
+        if constexpr (AMODE == A_F16_SMEM) {
+          const int s = kb % ST;
+          if (!mbar_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) break;
+          mbar_arrive_expect_tx(&full_bar[s], BM * BK * 2);
+          tma_load_2d(smem + s * C::STAGE, &tmap_a, kb * BK, m0, &full_bar[s]);
+          mbar_arrive_expect_tx(&rfull_bar[rs], C::B_RAW);
+          tma_load_2d(raw, &tmap_b, kb * C::B_RAW_ROW, n0, &rfull_bar[rs]);
         } else {
-          pa[i].v = make_uint4(0, 0, 0, 0);
+          mbar_arrive_expect_tx(&rfull_bar[rs], C::A_RAW + C::B_RAW);
+          tma_load_2d(raw, &tmap_a, kb * BK, m0, &rfull_bar[rs]);
+          tma_load_2d(raw + C::A_RAW, &tmap_b, kb * C::B_RAW_ROW, n0, &rfull_bar[rs]);
         }
+        issued = kb + 1;
       }
-#pragma unroll
-      for (int i = 0; i < C::NPB; ++i) {
-        const int pi = c + i * CONV_THREADS;
-        const int r = pi / C::B_PIECES_ROW, sub = pi % C::B_PIECES_ROW;
-        if (pi < C::B_PIECES && n0 + r < N) {
-          pb[i].v = __ldg(reinterpret_cast<const uint4*>(b_ptr + (size_t)(n0 + r) * b_row_stride +
-                                                          (size_t)kb * C::B_ROW_BYTES + sub * 16));
-        } else {
-          // zero codes: 0 for int8, and a zero word converts to zero for 4 / 2 bits
-          pb[i].v = make_uint4(0, 0, 0, 0);
-        }
-      }
-    };
-
-    auto store_kb = [&](uint8_t* stage, const RawPiece (&pa)[C::NPA], const RawPiece (&pb)[C::NPB]) {
-      uint8_t* ta = stage;
-      uint8_t* tb = stage + C::A_TILE;
-#pragma unroll
-      for (int i = 0; i < C::NPA; ++i) {
-        const int pi = c + i * CONV_THREADS;
-        if (pi >= C::A_PIECES) continue;
-        const int r = pi / C::A_PIECES_ROW, sub = pi % C::A_PIECES_ROW;
-        if constexpr (ACT == ACT_F16) {
-          st_chunk(ta, r, sub, pa[i].v);
-        } else {
-          uint4 o0, o1;
-          cvt_i8x4_f16(pa[i].v.x, o0.x, o0.y);
-          cvt_i8x4_f16(pa[i].v.y, o0.z, o0.w);
-          cvt_i8x4_f16(pa[i].v.z, o1.x, o1.y);
-          cvt_i8x4_f16(pa[i].v.w, o1.z, o1.w);
-          st_chunk(ta, r, 2 * sub, o0);
-          st_chunk(ta, r, 2 * sub + 1, o1);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < C::NPB; ++i) {
-        const int pi = c + i * CONV_THREADS;
-        if (pi >= C::B_PIECES) continue;
-        const int r = pi / C::B_PIECES_ROW, sub = pi % C::B_PIECES_ROW;
-        const uint32_t wv[4] = {pb[i].v.x, pb[i].v.y, pb[i].v.z, pb[i].v.w};
-        if constexpr (BBITS == 8) {
-          uint4 o0, o1;
-          cvt_i8x4_f16(wv[0], o0.x, o0.y);
-          cvt_i8x4_f16(wv[1], o0.z, o0.w);
-          cvt_i8x4_f16(wv[2], o1.x, o1.y);
-          cvt_i8x4_f16(wv[3], o1.z, o1.w);
-          st_chunk(tb, r, 2 * sub, o0);
-          st_chunk(tb, r, 2 * sub + 1, o1);
-        } else if constexpr (BBITS == 4) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t h[4];
-            cvt_i4x8_f16(INTER ? wv[j] : plain_to_inter_i4(wv[j]), h);
-            st_chunk(tb, r, 4 * sub + j, make_uint4(h[0], h[1], h[2], h[3]));
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t h[8];
-            cvt_i2x16_f16(INTER ? wv[j] : plain_to_inter_i2(wv[j]), h);
-            st_chunk(tb, r, 8 * sub + 2 * j, make_uint4(h[0], h[1], h[2], h[3]));
-            st_chunk(tb, r, 8 * sub + 2 * j + 1, make_uint4(h[4], h[5], h[6], h[7]));
-          }
-        }
-      }
-    };
-
-#pragma unroll
-    for (int p = 0; p < C::PF; ++p)
-      if (p < nkb) load_kb(p, ra[p], rb[p]);
-
-    bool ok = true;
-    for (int kb0 = 0; kb0 < nkb && ok; kb0 += C::PF) {
-#pragma unroll
-      for (int p = 0; p < C::PF; ++p) {
-        const int kb = kb0 + p;
-        if (kb < nkb && ok) {
-          const int s = kb % STAGES;
-          const uint32_t par = ((kb / STAGES) & 1) ^ 1;
-          const bool w_ok = mbar_wait(&empty_bar[s], par, timeout_ns, status);
-          if (!__all_sync(0xffffffffu, w_ok)) {
-            ok = false;
-          } else {
-            store_kb(smem + s * C::STAGE_BYTES, ra[p], rb[p]);
-            fence_proxy_async_smem();
-            mbar_arrive(&full_bar[s]);
-            if (kb + C::PF < nkb) load_kb(kb + C::PF, ra[p], rb[p]);
-          }
-        }
+      // no TMA write may land after the CTA has exited
+      for (int kb = issued > RST ? issued - RST : 0; kb < issued; ++kb)
+        mbar_wait(&rfull_bar[kb % RST], (kb / RST) & 1, DRAIN_TIMEOUT_NS, status);
+      if constexpr (AMODE == A_F16_SMEM) {
+        for (int kb = issued > ST ? issued - ST : 0; kb < issued; ++kb)
+          mbar_wait(&full_bar[kb % ST], (kb / ST) & 1, DRAIN_TIMEOUT_NS, status);
       }
     }
+    __syncwarp();
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(BM, BN);
+      const uint32_t smem_base = smem_u32(smem);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % ST;
+        if (!mbar_wait(&full_bar[s], (kb / ST) & 1, timeout_ns, status)) break;
+        tc_fence_after();
+        const int slice = (int)(((long long)kb * NACC) / nkb);
+        const bool first = kb == 0 || slice != (int)(((long long)(kb - 1) * NACC) / nkb);
+        const uint32_t d = tmem + (uint32_t)(slice * BN);
+        const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::STAGE + C::A_TILE);
+        if constexpr (AMODE == A_F16_SMEM) {
+          const uint64_t adesc = smem_desc_sw128(smem_base + s * C::STAGE);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K = +2 in the address field
+            tc_mma_f16(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+        } else {
+          const uint32_t a_tm = tmem + (uint32_t)(C::ACC_COLS + s * C::A_COLS);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)   // 16 k = 8 TMEM columns of A
+            tc_mma_f16_ts(d, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+        }
+        tc_commit(&empty_bar[s]);
+      }
+      tc_commit(accum_bar);
+      // no MMA may still be running when the tensor memory is freed
+      mbar_wait(accum_bar, 0, DRAIN_TIMEOUT_NS, status);
+    }
+    __syncwarp();
+  } else if (warp < C::A_WARPS) {
+    // ------------------------------------------------------------ int8 A -> TMEM
+    const int r = warp * 32 + lane;                       // tile row == TMEM lane
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int rs = kb % RST;
+      if (!warp_wait(&rfull_bar[rs], (kb / RST) & 1, timeout_ns, status)) break;
+      const uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE;
+      uint4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)   // 64B swizzle: chunk j of row r at j ^ ((r >> 1) & 3)
+        v[j] = *reinterpret_cast<const uint4*>(raw + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+      mbar_arrive(&rempty_bar[rs]);
+      uint32_t h[32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        cvt_i8x4_f16(v[j].x, h[8 * j + 0], h[8 * j + 1]);
+        cvt_i8x4_f16(v[j].y, h[8 * j + 2], h[8 * j + 3]);
+        cvt_i8x4_f16(v[j].z, h[8 * j + 4], h[8 * j + 5]);
+        cvt_i8x4_f16(v[j].w, h[8 * j + 6], h[8 * j + 7]);
+      }
+      const int s = kb % ST;
+      if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) break;
+      tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(C::ACC_COLS + s * C::A_COLS), h);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&full_bar[s]);
+    }
+  } else {
+    // ------------------------------------------------------------ weights -> fp16 smem
+    const int c = tid - C::A_WARPS * 32;
+    bool ok = true;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int rs = kb % RST;
+      if (!warp_wait(&rfull_bar[rs], (kb / RST) & 1, timeout_ns, status)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE + C::A_RAW;
+      uint4 v[C::NPB];
+#pragma unroll
+      for (int i = 0; i < C::NPB; ++i) {
+        const int pi = c + i * B_THREADS;
+        v[i] = pi < C::B_PIECES ? *reinterpret_cast<const uint4*>(raw + pi * 16) : make_uint4(0, 0, 0, 0);
+      }
+      mbar_arrive(&rempty_bar[rs]);
+      const int s = kb % ST;
+      if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) {
+        ok = false;
+        break;
+      }
+      uint8_t* tb = smem + s * C::STAGE + C::A_TILE;
+#pragma unroll
+      for (int i = 0; i < C::NPB; ++i) {
+        const int pi = c + i * B_THREADS;
+        if (pi < C::B_PIECES) convert_b_piece<BBITS, INTER>(tb, pi / C::B_PIECES_ROW, pi % C::B_PIECES_ROW, v[i]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&full_bar[s]);
+    }
 
-    // ------------------------------------------------------------------ epilogue
-    const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(accum_bar, 0, ok ? timeout_ns : 0, status));
+    // ------------------------------------------------------------ epilogue
+    const bool acc_ok = warp_wait(accum_bar, 0, ok ? timeout_ns : 0, status);
     tc_fence_after();
     if (acc_ok) {
-      const int q = warp & 3;                 // TMEM lane quadrant of this warp
-      const int chalf = warp >> 2;            // column half
+      const int q = warp & 3;                           // TMEM lane quadrant of this warp
+      const int chalf = (warp - C::A_WARPS) >> 2;       // column half
       const int row = m0 + 32 * q + lane;
       const bool row_ok = row < M;
       float rsc = 1.0f;
@@ -280,13 +354,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float f = __uint_as_float(r[i]);
-            if (a == 0) {
-              v[i] = f;
-              iv[i] = __float2int_rn(f);
-            } else {
-              v[i] += f;
-              iv[i] += __float2int_rn(f);
-            }
+            v[i] = a == 0 ? f : v[i] + f;
+            iv[i] = a == 0 ? __float2int_rn(f) : iv[i] + __float2int_rn(f);
           }
         }
         const int ncol = n0 + col;
@@ -299,8 +368,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t hv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              float x0 = __fmul_rn(v[2 * i], __half2float(col_scale[ncol + 2 * i]));
-              float x1 = __fmul_rn(v[2 * i + 1], __half2float(col_scale[ncol + 2 * i + 1]));
+              const __half2 sc2 = *reinterpret_cast<const __half2*>(col_scale + ncol + 2 * i);
+              float x0 = __fmul_rn(v[2 * i], __low2float(sc2));
+              float x1 = __fmul_rn(v[2 * i + 1], __high2float(sc2));
               if (epi == EPI_F16_ROWCOL) {
                 x0 = __fmul_rn(x0, rsc);
                 x1 = __fmul_rn(x1, rsc);
@@ -315,347 +385,79 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
     }
-  } else {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(BM, BN);
-      const uint32_t smem_base = smem_u32(smem);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % STAGES;
-        if (!mbar_wait(&full_bar[s], (kb / STAGES) & 1, timeout_ns, status)) break;
-        tc_fence_after();
-        const int slice = (int)(((long long)kb * NACC) / nkb);
-        const bool first = kb == 0 || slice != (int)(((long long)(kb - 1) * NACC) / nkb);
-        const uint32_t d = tmem + (uint32_t)(slice * BN);
-        const uint32_t sa = smem_base + s * C::STAGE_BYTES;
-        const uint64_t adesc = smem_desc_sw128(sa);
-        const uint64_t bdesc = smem_desc_sw128(sa + C::A_TILE);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          // +32 bytes along K per 16-element step = +2 in the descriptor's address field
-          tc_mma_f16(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
-        }
-        tc_commit(&empty_bar[s]);
-      }
-      tc_commit(accum_bar);
-      // make sure no MMA is still in flight before the tensor memory is freed
-      mbar_wait(accum_bar, 0, DRAIN_TIMEOUT_NS, status);
-    }
-    __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == CONV_WARPS) {
+  if (warp == C::MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, C::NCOLS);
   }
 }
 
 // ---------------------------------------------------------------------------
-// Variant with the int8 activations in tensor memory ("TA").  Converting A
-// into shared memory costs a store and an MMA read of every A element; here
-// 4 warps (one thread per tile row, which is exactly the TMEM lane that row
-// occupies) convert their row's 64 codes of a k-block to 32 fp16 pairs and
-// write them with tcgen05.st into a TMEM stage; the MMA reads A from TMEM
-// (the [a_tmem] operand form) and only B passes through shared memory.
-//   warps 0-3   A converters (TMEM writers)
-//   warps 4-11  B converters (swizzled shared-memory tiles), then the epilogue
-//   warp 12     tensor-memory allocation and the MMA issuer (lane 0)
+// Host side: tensor maps and launch
 // ---------------------------------------------------------------------------
-constexpr int TA_A_WARPS = 4;
-constexpr int TA_B_WARPS = 8;
-constexpr int TA_B_THREADS = TA_B_WARPS * 32;
-constexpr int TA_THREADS = (TA_A_WARPS + TA_B_WARPS + 1) * 32;
-
-template <int BBITS, int BN, int STAGES>
-struct TaCfg {
-  static constexpr int B_ROW_BYTES = BK * BBITS / 8;
-  static constexpr int B_PIECES_ROW = B_ROW_BYTES / 16;
-  static constexpr int B_PIECES = BN * B_PIECES_ROW;
-  static constexpr int NPB = (B_PIECES + TA_B_THREADS - 1) / TA_B_THREADS;
-  static constexpr int B_TILE = BN * 128;
-  static constexpr int A_COLS = BK / 2;                    // TMEM columns per A stage
-  static constexpr int NCOLS = 512;
-  static constexpr int PF = 4;
-  static constexpr size_t SMEM = (size_t)STAGES * B_TILE + 1024 + 256;
-  static_assert(BN + STAGES * A_COLS <= NCOLS, "TMEM budget");
-};
-
-template <int BBITS, int BN, bool INTER, int STAGES>
-__global__ void __launch_bounds__(TA_THREADS, 1)
-    gemm_tc_ta_kernel(const int8_t* __restrict__ a_ptr, const uint8_t* __restrict__ b_ptr, int M, int N, int K,
-                      const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
-                      void* __restrict__ out, uint64_t timeout_ns, int* status) {
-  using C = TaCfg<BBITS, BN, STAGES>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * C::B_TILE);
-  uint64_t* empty_bar = full_bar + STAGES;
-  uint64_t* accum_bar = empty_bar + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.y * BM;
-  const int n0 = blockIdx.x * BN;
-  const int nkb = K / BK;
-  constexpr int MMA_WARP = TA_A_WARPS + TA_B_WARPS;
-
-  if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], TA_A_WARPS * 32 + TA_B_THREADS);
-      mbar_init(&empty_bar[s], 1);
-    }
-    mbar_init(accum_bar, 1);
-    mbar_fence_init();
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
-  if (warp == MMA_WARP) {
-    tmem_alloc(tmem_slot, C::NCOLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp < TA_A_WARPS) {
-    // ------------------------------------------------------------ A -> TMEM
-    const int row = m0 + warp * 32 + lane;
-    const bool row_ok = row < M;
-    const uint4* arow = reinterpret_cast<const uint4*>(a_ptr + (size_t)(row_ok ? row : 0) * K);
-    uint4 ra[C::PF][4];
-    auto load_a = [&](int kb, uint4 (&v)[4]) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = row_ok ? __ldg(arow + kb * 4 + j) : make_uint4(0, 0, 0, 0);
-    };
-#pragma unroll
-    for (int p = 0; p < C::PF; ++p)
-      if (p < nkb) load_a(p, ra[p]);
-    bool ok = true;
-    for (int kb0 = 0; kb0 < nkb && ok; kb0 += C::PF) {
-#pragma unroll
-      for (int p = 0; p < C::PF; ++p) {
-        const int kb = kb0 + p;
-        if (kb < nkb && ok) {
-          uint32_t h[32];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            cvt_i8x4_f16(ra[p][j].x, h[8 * j + 0], h[8 * j + 1]);
-            cvt_i8x4_f16(ra[p][j].y, h[8 * j + 2], h[8 * j + 3]);
-            cvt_i8x4_f16(ra[p][j].z, h[8 * j + 4], h[8 * j + 5]);
-            cvt_i8x4_f16(ra[p][j].w, h[8 * j + 6], h[8 * j + 7]);
-          }
-          if (kb + C::PF < nkb) load_a(kb + C::PF, ra[p]);
-          const int s = kb % STAGES;
-          const bool w_ok = mbar_wait(&empty_bar[s], ((kb / STAGES) & 1) ^ 1, timeout_ns, status);
-          if (!__all_sync(0xffffffffu, w_ok)) {
-            ok = false;
-          } else {
-            tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(BN + s * C::A_COLS), h);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&full_bar[s]);
-          }
-        }
-      }
-    }
-  } else if (warp < MMA_WARP) {
-    // ------------------------------------------------------------ B -> smem
-    const int c = tid - TA_A_WARPS * 32;
-    const size_t b_row_stride = (size_t)K * BBITS / 8;
-    uint4 rb[C::PF][C::NPB];
-    auto load_b = [&](int kb, uint4 (&v)[C::NPB]) {
-#pragma unroll
-      for (int i = 0; i < C::NPB; ++i) {
-        const int pi = c + i * TA_B_THREADS;
-        const int r = pi / C::B_PIECES_ROW, sub = pi % C::B_PIECES_ROW;
-        v[i] = (pi < C::B_PIECES && n0 + r < N)
-                   ? __ldg(reinterpret_cast<const uint4*>(b_ptr + (size_t)(n0 + r) * b_row_stride +
-                                                          (size_t)kb * C::B_ROW_BYTES + sub * 16))
-                   : make_uint4(0, 0, 0, 0);
-      }
-    };
-    auto store_b = [&](uint8_t* tb, const uint4 (&v)[C::NPB]) {
-#pragma unroll
-      for (int i = 0; i < C::NPB; ++i) {
-        const int pi = c + i * TA_B_THREADS;
-        if (pi >= C::B_PIECES) continue;
-        const int r = pi / C::B_PIECES_ROW, sub = pi % C::B_PIECES_ROW;
-        const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        if constexpr (BBITS == 8) {
-          uint4 o0, o1;
-          cvt_i8x4_f16(wv[0], o0.x, o0.y);
-          cvt_i8x4_f16(wv[1], o0.z, o0.w);
-          cvt_i8x4_f16(wv[2], o1.x, o1.y);
-          cvt_i8x4_f16(wv[3], o1.z, o1.w);
-          st_chunk(tb, r, 2 * sub, o0);
-          st_chunk(tb, r, 2 * sub + 1, o1);
-        } else if constexpr (BBITS == 4) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t h[4];
-            cvt_i4x8_f16(INTER ? wv[j] : plain_to_inter_i4(wv[j]), h);
-            st_chunk(tb, r, 4 * sub + j, make_uint4(h[0], h[1], h[2], h[3]));
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t h[8];
-            cvt_i2x16_f16(INTER ? wv[j] : plain_to_inter_i2(wv[j]), h);
-            st_chunk(tb, r, 8 * sub + 2 * j, make_uint4(h[0], h[1], h[2], h[3]));
-            st_chunk(tb, r, 8 * sub + 2 * j + 1, make_uint4(h[4], h[5], h[6], h[7]));
-          }
-        }
-      }
-    };
-#pragma unroll
-    for (int p = 0; p < C::PF; ++p)
-      if (p < nkb) load_b(p, rb[p]);
-    bool ok = true;
-    for (int kb0 = 0; kb0 < nkb && ok; kb0 += C::PF) {
-#pragma unroll
-      for (int p = 0; p < C::PF; ++p) {
-        const int kb = kb0 + p;
-        if (kb < nkb && ok) {
-          const int s = kb % STAGES;
-          const bool w_ok = mbar_wait(&empty_bar[s], ((kb / STAGES) & 1) ^ 1, timeout_ns, status);
-          if (!__all_sync(0xffffffffu, w_ok)) {
-            ok = false;
-          } else {
-            store_b(smem + s * C::B_TILE, rb[p]);
-            fence_proxy_async_smem();
-            mbar_arrive(&full_bar[s]);
-            if (kb + C::PF < nkb) load_b(kb + C::PF, rb[p]);
-          }
-        }
-      }
-    }
-
-    // ------------------------------------------------------------ epilogue
-    const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(accum_bar, 0, ok ? timeout_ns : 0, status));
-    tc_fence_after();
-    if (acc_ok) {
-      const int q = warp & 3;                       // TMEM lane quadrant of this warp
-      const int chalf = (warp - TA_A_WARPS) >> 2;   // column half
-      const int row = m0 + 32 * q + lane;
-      const bool row_ok = row < M;
-      float rsc = 1.0f;
-      if (epi == EPI_F16_ROWCOL && row_ok) rsc = __half2float(row_scale[row]);
-#pragma unroll 1
-      for (int cc = 0; cc < BN / 64; ++cc) {
-        const int col = chalf * (BN / 2) + cc * 32;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
-        tmem_ld_wait();
-        const int ncol = n0 + col;
-        if (row_ok && ncol < N) {
-          if (epi == EPI_I32) {
-            int4* dst = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + (size_t)row * N + ncol);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_int4(__float2int_rn(__uint_as_float(r[4 * i])), __float2int_rn(__uint_as_float(r[4 * i + 1])),
-                                 __float2int_rn(__uint_as_float(r[4 * i + 2])),
-                                 __float2int_rn(__uint_as_float(r[4 * i + 3])));
-          } else {
-            uint32_t hv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float x0 = __fmul_rn(__uint_as_float(r[2 * i]), __half2float(col_scale[ncol + 2 * i]));
-              float x1 = __fmul_rn(__uint_as_float(r[2 * i + 1]), __half2float(col_scale[ncol + 2 * i + 1]));
-              if (epi == EPI_F16_ROWCOL) {
-                x0 = __fmul_rn(x0, rsc);
-                x1 = __fmul_rn(x1, rsc);
-              }
-              const __half2 h2 = __halves2half2(__float2half_rn(x0), __float2half_rn(x1));
-              hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(out) + (size_t)row * N + ncol);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
-          }
-        }
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(BM, BN);
-      const uint32_t smem_base = smem_u32(smem);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % STAGES;
-        if (!mbar_wait(&full_bar[s], (kb / STAGES) & 1, timeout_ns, status)) break;
-        tc_fence_after();
-        const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::B_TILE);
-        const uint32_t a_tm = tmem + (uint32_t)(BN + s * C::A_COLS);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          // 16 k = 8 TMEM columns of A; 32 bytes along K in the swizzled B tile
-          tc_mma_f16_ts(tmem, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (kb == 0 && kk == 0) ? 0u : 1u);
-        }
-        tc_commit(&empty_bar[s]);
-      }
-      tc_commit(accum_bar);
-      mbar_wait(accum_bar, 0, DRAIN_TIMEOUT_NS, status);
-    }
-    __syncwarp();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == MMA_WARP) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::NCOLS);
-  }
+  return fn;
 }
 
-template <int BBITS, int BN, bool INTER>
-cudaError_t launch_ta(const GemmArgs& g, cudaStream_t stream) {
-  constexpr int STAGES = 4;
-  using C = TaCfg<BBITS, BN, STAGES>;
-  int* status = nullptr;
-  cudaError_t se = device_status_ptr(&status);
-  if (se != cudaSuccess) return se;
-  auto kern = gemm_tc_ta_kernel<BBITS, BN, INTER, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
-  kern<<<grid, TA_THREADS, C::SMEM, stream>>>(static_cast<const int8_t*>(g.a), static_cast<const uint8_t*>(g.b),
-                                              (int)g.M, (int)g.N, (int)g.K,
-                                              reinterpret_cast<const __half*>(g.row_scale),
-                                              reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c,
-                                              (uint64_t)wait_timeout_ns(), status);
-  return cudaGetLastError();
+// 2-D map over a row-major matrix of `rows` rows of `row_elems` elements
+// (uint8, or fp16 when elem == 2); box = box_x elements x box_rows rows.
+// Out-of-range rows read as zero.
+cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_elems, uint64_t rows, uint32_t box_x,
+                     uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {row_elems, rows};
+  const cuuint64_t strides[1] = {row_elems * (uint64_t)elem};
+  const cuuint32_t box[2] = {box_x, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int BBITS, int BN>
-cudaError_t launch_ta_layout(const GemmArgs& g, cudaStream_t stream) {
-  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_ta<BBITS, BN, false>(g, stream);
-  return launch_ta<BBITS, BN, true>(g, stream);
-}
-
-template <int ACT, int BBITS, int BN, int NACC, bool INTER>
+template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST>
 cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
-  constexpr int STAGES = 4;
+  using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST>;
   int* status = nullptr;
-  cudaError_t se = device_status_ptr(&status);
-  if (se != cudaSuccess) return se;
-  using C = TcCfg<ACT, BBITS, BN, NACC, INTER, STAGES>;
-  auto kern = gemm_tc_kernel<ACT, BBITS, BN, NACC, INTER, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  cudaError_t e = device_status_ptr(&status);
+  if (e != cudaSuccess) return e;
+  CUtensorMap ma, mb;
+  if (AMODE == A_F16_SMEM) {
+    e = make_map(&ma, g.a, 2, (uint64_t)g.K, (uint64_t)g.M, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    e = make_map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, BK, BM, CU_TENSOR_MAP_SWIZZLE_64B);
+  }
+  if (e != cudaSuccess) return e;
+  e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_RAW_ROW, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (e != cudaSuccess) return e;
+  auto kern = gemm_tc_kernel<AMODE, BBITS, BN, NACC, INTER, ST, RST>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
-  kern<<<grid, TC_THREADS, C::SMEM, stream>>>(g.a, static_cast<const uint8_t*>(g.b), (int)g.M, (int)g.N, (int)g.K,
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(ma, mb, (int)g.M, (int)g.N, (int)g.K,
                                               reinterpret_cast<const __half*>(g.row_scale),
                                               reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c,
                                               (uint64_t)wait_timeout_ns(), status);
   return cudaGetLastError();
 }
 
-template <int ACT, int BBITS, int BN, int NACC>
+template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST>
 cudaError_t launch_layout(const GemmArgs& g, cudaStream_t stream) {
-  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_t<ACT, BBITS, BN, NACC, false>(g, stream);
-  return launch_t<ACT, BBITS, BN, NACC, true>(g, stream);
+  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_t<AMODE, BBITS, BN, NACC, false, ST, RST>(g, stream);
+  return launch_t<AMODE, BBITS, BN, NACC, true, ST, RST>(g, stream);
 }
 
 }  // namespace
@@ -663,24 +465,21 @@ cudaError_t launch_layout(const GemmArgs& g, cudaStream_t stream) {
 cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream) {
   const int nkb = (int)(g.K / BK);
   if (g.act == ACT_I8 && g.bbits == 8) {
-    // int32 output: slices of at most 1024 k keep every partial sum < 2**24 exactly
     if (g.epi == EPI_I32) {
-      if (nkb <= 16) return launch_layout<ACT_I8, 8, 256, 1>(g, stream);
-      if (nkb <= 32) return launch_layout<ACT_I8, 8, 256, 2>(g, stream);
-      if (nkb <= 64) return launch_layout<ACT_I8, 8, 128, 4>(g, stream);
+      // int32 output: slices of at most 1024 k keep every partial sum < 2**24 exactly
+      if (nkb <= 16) return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 4>(g, stream);
+      if (nkb <= 32) return launch_layout<A_I8_TMEM, 8, 128, 2, 4, 4>(g, stream);
+      if (nkb <= 64) return launch_layout<A_I8_TMEM, 8, 64, 4, 4, 4>(g, stream);
       return cudaErrorInvalidValue;
     }
-    return launch_ta_layout<8, 256>(g, stream);
+    return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 4>(g, stream);
   }
   // int8 activations with 4- / 2-bit weights: every partial sum < 2**24 (host-bounded K)
-  if (g.act == ACT_I8 && g.bbits == 4) return launch_ta_layout<4, 256>(g, stream);
-  if (g.act == ACT_I8 && g.bbits == 2) return launch_ta_layout<2, 256>(g, stream);
-  // fp16 activations: the accumulator is not an exact integer, so K is split
-  // into two separately accumulated halves (shorter fp32 accumulation chains
-  // in the tensor core), summed in fp32 in the epilogue.
+  if (g.act == ACT_I8 && g.bbits == 4) return launch_layout<A_I8_TMEM, 4, 256, 1, 4, 5>(g, stream);
+  if (g.act == ACT_I8 && g.bbits == 2) return launch_layout<A_I8_TMEM, 2, 256, 1, 4, 6>(g, stream);
   if (g.act == ACT_F16 && g.bbits == 4) {
-    if (nkb >= 2) return launch_layout<ACT_F16, 4, 256, 2>(g, stream);
-    return launch_layout<ACT_F16, 4, 256, 1>(g, stream);
+    if (nkb >= 2) return launch_layout<A_F16_SMEM, 4, 256, 2, 3, 8>(g, stream);
+    return launch_layout<A_F16_SMEM, 4, 256, 1, 3, 8>(g, stream);
   }
   return cudaErrorInvalidValue;
 }
