@@ -21,13 +21,13 @@
 //   producer warp  one thread issues 2-D TMA loads (cp.async.bulk.tensor) of
 //                  the raw k-blocks of B (and of A) into a ring of RST raw
 //                  stages; rows past M / N arrive zero-filled.
-//   A warps (4)    int8 activations only: thread = tile row = TMEM lane; reads
+//   A warps (4/group) int8 activations only: thread = tile row = TMEM lane; reads
 //                  its 64 raw codes (64B-swizzled, conflict-free), converts
 //                  them to 32 fp16 pairs and writes them with tcgen05.st into
 //                  a TMEM stage that the MMA reads as its A operand.
 //                  fp16 activations need no conversion: the producer loads
 //                  them with TMA straight into the 128B-swizzled MMA layout.
-//   B warps (8)    read raw weight codes, convert them to fp16 and store the
+//   B warps (8/group) read raw weight codes, convert them to fp16 and store the
 //                  128B-swizzled K-major tile the MMA reads; after the
 //                  mainloop they run the epilogue (TMEM -> registers -> HBM).
 //   MMA warp       allocates tensor memory; lane 0 issues 4 MMAs per 64-wide
@@ -83,15 +83,20 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;                 // k per block: one 128-byte fp16 swizzle row
-constexpr int B_WARPS = 8;
-constexpr int B_THREADS = B_WARPS * 32;
+constexpr int B_THREADS = 256;         // one weight-converter group (8 warps) per k-block
 constexpr uint64_t DRAIN_TIMEOUT_NS = 4000000000ull;
 
 enum AMode : int { A_I8_TMEM = 0, A_F16_SMEM = 1 };
 
-template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST>
+// Converter groups per CTA.
+constexpr int TC_NG = 2;
+
+// NG converter groups take the k-blocks in turn (group g converts k-blocks
+// kb = g (mod NG)), so conversion of consecutive k-blocks overlaps.
+template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST, int NG>
 struct Cfg {
-  static constexpr int A_WARPS = AMODE == A_I8_TMEM ? 4 : 0;
+  static constexpr int A_WARPS = AMODE == A_I8_TMEM ? 4 * NG : 0;
+  static constexpr int B_WARPS = 8 * NG;
   static constexpr int MMA_WARP = A_WARPS + B_WARPS;
   static constexpr int PRODUCER_WARP = MMA_WARP + 1;
   static constexpr int THREADS = (PRODUCER_WARP + 1) * 32;
@@ -116,6 +121,7 @@ struct Cfg {
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(STAGE % 1024 == 0 && RSTAGE % 1024 == 0, "stage alignment");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert((BN / (2 * NG)) % 32 == 0, "epilogue column parts are whole 32-column chunks");
 };
 
 // Store one 16-byte fp16 chunk (logical chunk lc = 8 k values) of row r into a
@@ -160,12 +166,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, timeout_ns, status));
 }
 
-template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST>
-__global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST>::THREADS, 1)
+template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST, int NG>
+__global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
                    int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
                    void* __restrict__ out, uint64_t timeout_ns, int* status) {
-  using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST>;
+  using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);   // MMA stage ready
@@ -180,7 +186,8 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST>::THREADS,
   const int m0 = blockIdx.y * BM;
   const int n0 = blockIdx.x * BN;
   const int nkb = K / BK;
-  constexpr int CONSUMERS = (C::A_WARPS + B_WARPS) * 32;
+  // threads that consume one k-block: one A group (4 warps) and one B group (8 warps)
+  constexpr int CONSUMERS = (C::A_WARPS / NG + 8) * 32;
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -272,8 +279,9 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST>::THREADS,
     __syncwarp();
   } else if (warp < C::A_WARPS) {
     // ------------------------------------------------------------ int8 A -> TMEM
-    const int r = warp * 32 + lane;                       // tile row == TMEM lane
-    for (int kb = 0; kb < nkb; ++kb) {
+    const int q = warp & 3;                               // TMEM lane quadrant
+    const int r = q * 32 + lane;                          // tile row == TMEM lane
+    for (int kb = warp >> 2; kb < nkb; kb += NG) {
       const int rs = kb % RST;
       if (!warp_wait(&rfull_bar[rs], (kb / RST) & 1, timeout_ns, status)) break;
       const uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE;
@@ -292,16 +300,17 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST>::THREADS,
       }
       const int s = kb % ST;
       if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) break;
-      tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(C::ACC_COLS + s * C::A_COLS), h);
+      tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::ACC_COLS + s * C::A_COLS), h);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&full_bar[s]);
     }
   } else {
     // ------------------------------------------------------------ weights -> fp16 smem
-    const int c = tid - C::A_WARPS * 32;
+    const int bw = warp - C::A_WARPS;                     // 0 .. 8 * NG - 1
+    const int c = (bw & 7) * 32 + lane;                   // thread within its group
     bool ok = true;
-    for (int kb = 0; kb < nkb; ++kb) {
+    for (int kb = bw >> 3; kb < nkb; kb += NG) {
       const int rs = kb % RST;
       if (!warp_wait(&rfull_bar[rs], (kb / RST) & 1, timeout_ns, status)) {
         ok = false;
@@ -334,15 +343,17 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST>::THREADS,
     const bool acc_ok = warp_wait(accum_bar, 0, ok ? timeout_ns : 0, status);
     tc_fence_after();
     if (acc_ok) {
+      // 2 * NG warps share each TMEM lane quadrant; each takes a column part
       const int q = warp & 3;                           // TMEM lane quadrant of this warp
-      const int chalf = (warp - C::A_WARPS) >> 2;       // column half
+      const int cpart = bw >> 2;                        // 0 .. 2 * NG - 1
+      constexpr int PART = BN / (2 * NG);
       const int row = m0 + 32 * q + lane;
       const bool row_ok = row < M;
       float rsc = 1.0f;
       if (epi == EPI_F16_ROWCOL && row_ok) rsc = __half2float(row_scale[row]);
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 64; ++cc) {
-        const int col = chalf * (BN / 2) + cc * 32;
+      for (int cc = 0; cc < PART / 32; ++cc) {
+        const int col = cpart * PART + cc * 32;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col;
         uint32_t r[32];
         float v[32];
@@ -428,9 +439,9 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST>
+template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST, int NG>
 cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
-  using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST>;
+  using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG>;
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
@@ -443,7 +454,7 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_RAW_ROW, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_tc_kernel<AMODE, BBITS, BN, NACC, INTER, ST, RST>;
+  auto kern = gemm_tc_kernel<AMODE, BBITS, BN, NACC, INTER, ST, RST, NG>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
@@ -454,10 +465,11 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST>
+template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST, int NG = TC_NG>
 cudaError_t launch_layout(const GemmArgs& g, cudaStream_t stream) {
-  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_t<AMODE, BBITS, BN, NACC, false, ST, RST>(g, stream);
-  return launch_t<AMODE, BBITS, BN, NACC, true, ST, RST>(g, stream);
+  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN)
+    return launch_t<AMODE, BBITS, BN, NACC, false, ST, RST, NG>(g, stream);
+  return launch_t<AMODE, BBITS, BN, NACC, true, ST, RST, NG>(g, stream);
 }
 
 }  // namespace
@@ -469,7 +481,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream) {
       // int32 output: slices of at most 1024 k keep every partial sum < 2**24 exactly
       if (nkb <= 16) return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 4>(g, stream);
       if (nkb <= 32) return launch_layout<A_I8_TMEM, 8, 128, 2, 4, 4>(g, stream);
-      if (nkb <= 64) return launch_layout<A_I8_TMEM, 8, 64, 4, 4, 4>(g, stream);
+      if (nkb <= 64) return launch_layout<A_I8_TMEM, 8, 64, 4, 4, 4, 1>(g, stream);
       return cudaErrorInvalidValue;
     }
     return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 4>(g, stream);

@@ -4,9 +4,11 @@
 // use of the quantised linear in "BMINF的後訓練量化實現", 實現代碼分析2, runs
 // with M = batch).  A block of 4 warps owns 16 weight rows; each warp takes a
 // quarter of K.  Every thread first issues all of its 16-byte weight loads
-// (two rows, up to UNITS steps: ~8 KB per warp in flight); while they are in
-// flight the block stages the activations (at most 16 rows, as fp16; int8
-// activations are converted exactly on the way) into shared memory.  The
+// (two rows, up to UNITS steps: ~8 KB per warp in flight).  The activations
+// (at most 16 rows) are staged into shared memory with asynchronous copies
+// issued before the weight loads, so they never queue behind them; int8
+// activations are staged as bytes and converted exactly to fp16 when the
+// MMA operand is built.  The
 // codes are then turned into fp16 pairs in registers (exact) and fed straight
 // into mma.sync m16n8k16 as the A fragment, so weights never touch shared
 // memory.  Accumulation is fp32; for integer operands every partial sum stays
@@ -35,7 +37,7 @@ struct GemvCfg {
   static constexpr int STEP = 4 * E16;                // k per step (4 threads of a quad)
   static constexpr int PW = 16 / BBITS;               // fp16 pairs per 32-bit word
   static constexpr int KW = 32 / BBITS;               // k per 32-bit word
-  static constexpr int PAD = BBITS == 4 ? 16 : 64;    // staged activation row pad (bytes)
+  static constexpr int PAD = BBITS == 4 ? 16 : 64;    // staged fp16 activation row pad (bytes)
   // Chunk position inside a staged activation row.  Thread t of a quad reads
   // chunks [t * E16 / 8, (t + 1) * E16 / 8) of a step; with this swizzle and
   // the row pad the 8 threads of a quarter warp (2 rows x 4 quads) hit 8
@@ -45,9 +47,11 @@ struct GemvCfg {
   }
 };
 
-template <int BBITS>
-constexpr int gemv_smem_bytes(int M, int K) {
-  return M * (2 * K + GemvCfg<BBITS>::PAD);
+// Staged activation row stride: fp16 rows with the swizzle pad, or int8 rows
+// padded by 8 bytes (conflict-free 8-byte fragment loads).
+template <int BBITS, int ACT>
+__host__ __device__ constexpr int gemv_row_stride(int K) {
+  return ACT == ACT_F16 ? 2 * K + GemvCfg<BBITS>::PAD : K + 8;
 }
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -77,7 +81,22 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
   using C = GemvCfg<BBITS>;
   __shared__ float red[GEMV_WARPS][NB][4][32];
   extern __shared__ __align__(16) uint8_t xs[];       // M staged activation rows
-  const int rs = 2 * K + C::PAD;
+  const int rs = gemv_row_stride<BBITS, ACT>(K);
+
+  // ---- stage the activations asynchronously (they are small and L2 resident) ----
+  if constexpr (ACT == ACT_F16) {
+    const int chunks_per_row = K >> 3;                // 16-byte chunks of 8 fp16
+    for (int idx = threadIdx.x; idx < M * chunks_per_row; idx += blockDim.x) {
+      const int m = idx / chunks_per_row, c = idx - m * chunks_per_row;
+      cp_async_16(xs + (size_t)m * rs + C::swz(c) * 16, static_cast<const __half*>(act) + (size_t)m * K + 8 * c);
+    }
+  } else {
+    const int chunks_per_row = K >> 3;                // 8-byte chunks of 8 int8
+    for (int idx = threadIdx.x; idx < M * chunks_per_row; idx += blockDim.x) {
+      const int m = idx / chunks_per_row, c = idx - m * chunks_per_row;
+      cp_async_8(xs + (size_t)m * rs + 8 * c, static_cast<const int8_t*>(act) + (size_t)m * K + 8 * c);
+    }
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -113,21 +132,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
       }
     }
     if (first) {
-      // stage the activations while the first weight loads are in flight
-      const int chunks_per_row = K >> 3;
-      for (int idx = threadIdx.x; idx < M * chunks_per_row; idx += blockDim.x) {
-        const int m = idx / chunks_per_row, c = idx - m * chunks_per_row;
-        uint4 v;
-        if constexpr (ACT == ACT_F16) {
-          v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __half*>(act) + (size_t)m * K) + c);
-        } else {
-          const uint2 raw =
-              __ldg(reinterpret_cast<const uint2*>(static_cast<const int8_t*>(act) + (size_t)m * K) + c);
-          cvt_i8x4_f16(raw.x, v.x, v.y);
-          cvt_i8x4_f16(raw.y, v.z, v.w);
-        }
-        *reinterpret_cast<uint4*>(xs + (size_t)m * rs + C::swz(c) * 16) = v;
-      }
+      cp_async_wait_all();
       __syncthreads();
     }
 #pragma unroll
@@ -152,8 +157,17 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
             const int m = nb * 8 + g;
-            xb[nb] = (m < M && kin) ? *reinterpret_cast<const uint4*>(xs + (size_t)m * rs + C::swz(chunk) * 16)
-                                    : make_uint4(0, 0, 0, 0);
+            if (m < M && kin) {
+              if constexpr (ACT == ACT_F16) {
+                xb[nb] = *reinterpret_cast<const uint4*>(xs + (size_t)m * rs + C::swz(chunk) * 16);
+              } else {
+                const uint2 raw = *reinterpret_cast<const uint2*>(xs + (size_t)m * rs + 8 * chunk);
+                cvt_i8x4_f16(raw.x, xb[nb].x, xb[nb].y);
+                cvt_i8x4_f16(raw.y, xb[nb].z, xb[nb].w);
+              }
+            } else {
+              xb[nb] = make_uint4(0, 0, 0, 0);
+            }
           }
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
@@ -195,7 +209,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
 
 template <int BBITS, int ACT, int NB, bool INTER>
 cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
-  const int smem = gemv_smem_bytes<BBITS>((int)g.M, (int)g.K);
+  const int smem = (int)g.M * gemv_row_stride<BBITS, ACT>((int)g.K);
   auto kern = gemv_mma_kernel<BBITS, ACT, NB, INTER>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
