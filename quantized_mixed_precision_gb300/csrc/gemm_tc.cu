@@ -89,7 +89,7 @@ constexpr uint64_t DRAIN_TIMEOUT_NS = 4000000000ull;
 enum AMode : int { A_I8_TMEM = 0, A_F16_SMEM = 1 };
 
 // Converter groups per CTA.
-constexpr int TC_NG = 2;
+constexpr int TC_NG = 1;
 
 // NG converter groups take the k-blocks in turn (group g converts k-blocks
 // kb = g (mod NG)), so conversion of consecutive k-blocks overlaps.

@@ -37,13 +37,15 @@ struct GemvCfg {
   static constexpr int STEP = 4 * E16;                // k per step (4 threads of a quad)
   static constexpr int PW = 16 / BBITS;               // fp16 pairs per 32-bit word
   static constexpr int KW = 32 / BBITS;               // k per 32-bit word
+  static constexpr int CPT = E16 / 8;                 // 8-value activation chunks per thread per step
   static constexpr int PAD = BBITS == 4 ? 16 : 64;    // staged fp16 activation row pad (bytes)
-  // Chunk position inside a staged activation row.  Thread t of a quad reads
-  // chunks [t * E16 / 8, (t + 1) * E16 / 8) of a step; with this swizzle and
-  // the row pad the 8 threads of a quarter warp (2 rows x 4 quads) hit 8
-  // different 16-byte bank groups.
-  __device__ __forceinline__ static int swz(int c) {
-    return BBITS == 4 ? (c ^ (((c >> 3) & 1) << 1)) : (c ^ ((c >> 3) & 7));
+  // Position of 16-byte chunk j (0 <= j < CPT) of quad thread t inside one
+  // step of a staged fp16 row.  The XOR depends only on t, so every thread
+  // precomputes its offsets once; with the row pad, the 8 threads of a
+  // quarter warp (2 rows x 4 quad threads) hit 8 different bank groups.
+  __device__ __forceinline__ static int chunk_pos(int t, int j) {
+    const int c = t * CPT + j;
+    return BBITS == 4 ? (c ^ ((t >> 1) << 1)) : (c ^ t);
   }
 };
 
@@ -80,23 +82,27 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
                                                                       void* __restrict__ out) {
   using C = GemvCfg<BBITS>;
   __shared__ float red[GEMV_WARPS][NB][4][32];
-  extern __shared__ __align__(16) uint8_t xs[];       // M staged activation rows
+  extern __shared__ __align__(16) uint8_t xs[];       // M staged activation rows, then 16 zero bytes
   const int rs = gemv_row_stride<BBITS, ACT>(K);
+  uint8_t* const zero_chunk = xs + (size_t)M * rs;
 
   // ---- stage the activations asynchronously (they are small and L2 resident) ----
+  const int chunks_per_row = K >> 3;
   if constexpr (ACT == ACT_F16) {
-    const int chunks_per_row = K >> 3;                // 16-byte chunks of 8 fp16
     for (int idx = threadIdx.x; idx < M * chunks_per_row; idx += blockDim.x) {
       const int m = idx / chunks_per_row, c = idx - m * chunks_per_row;
-      cp_async_16(xs + (size_t)m * rs + C::swz(c) * 16, static_cast<const __half*>(act) + (size_t)m * K + 8 * c);
+      const int sstep = c / (C::STEP / 8), cin = c - sstep * (C::STEP / 8);   // step, chunk within the step
+      const int pos = C::chunk_pos(cin / C::CPT, cin % C::CPT);
+      cp_async_16(xs + (size_t)m * rs + (size_t)sstep * (C::STEP * 2) + pos * 16,
+                  static_cast<const __half*>(act) + (size_t)m * K + 8 * c);
     }
   } else {
-    const int chunks_per_row = K >> 3;                // 8-byte chunks of 8 int8
     for (int idx = threadIdx.x; idx < M * chunks_per_row; idx += blockDim.x) {
       const int m = idx / chunks_per_row, c = idx - m * chunks_per_row;
       cp_async_8(xs + (size_t)m * rs + 8 * c, static_cast<const int8_t*>(act) + (size_t)m * K + 8 * c);
     }
   }
+  if (threadIdx.x == 0) *reinterpret_cast<uint4*>(zero_chunk) = make_uint4(0, 0, 0, 0);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -108,11 +114,29 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
   const int s_begin = (warp * nsteps) / GEMV_WARPS;
   const int s_end = ((warp + 1) * nsteps) / GEMV_WARPS;
 
-  float d[NB][4];
+  // Per-thread activation fragment addressing: rows past M read the zero chunk.
+  const uint8_t* xrow[NB];
+  uint32_t xmask[NB];
 #pragma unroll
-  for (int nb = 0; nb < NB; ++nb)
+  for (int nb = 0; nb < NB; ++nb) {
+    const int m = nb * 8 + g;
+    xrow[nb] = m < M ? xs + (size_t)m * rs : zero_chunk;
+    xmask[nb] = m < M ? 0xffffffffu : 0u;
+  }
+  uint32_t xoff[C::CPT];        // byte offset of chunk j of this thread inside a step
 #pragma unroll
-    for (int i = 0; i < 4; ++i) d[nb][i] = 0.0f;
+  for (int j = 0; j < C::CPT; ++j)
+    xoff[j] = ACT == ACT_F16 ? (uint32_t)(C::chunk_pos(t, j) * 16) : (uint32_t)((t * C::CPT + j) * 8);
+  constexpr uint32_t STEP_BYTES = ACT == ACT_F16 ? C::STEP * 2 : C::STEP;
+
+  // Two independent accumulator chains per output block (even / odd words).
+  float d[2][NB][4];
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[a][nb][i] = 0.0f;
 
   // The first iteration always runs (every warp takes part in the staging
   // barrier, even one with no steps of its own).
@@ -139,10 +163,10 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
     for (int u = 0; u < UNITS; ++u) {
       const int s = s0 + u;
       if (s >= s_end) break;                                  // warp-uniform
-      // a ragged last step: threads past K hold zero codes and read zero
-      // activations (mma.sync needs the whole warp)
-      const int kbase = s * C::STEP + t * C::E16;
-      const bool kin = kbase < K;
+      // a ragged last step: threads past K hold zero codes and read the zero
+      // chunk (mma.sync needs the whole warp)
+      const bool kin = (s * C::STEP + t * C::E16) < K;
+      const uint32_t sbase = (uint32_t)s * STEP_BYTES;
       const uint32_t wa[4] = {v0[u].x, v0[u].y, v0[u].z, v0[u].w};
       const uint32_t wb[4] = {v1[u].x, v1[u].y, v1[u].z, v1[u].w};
 #pragma unroll
@@ -152,38 +176,35 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
         convert_word<BBITS, INTER>(wb[i], hb);
 #pragma unroll
         for (int c = 0; c < C::PW / 4; ++c) {
-          const int chunk = (kbase >> 3) + i * (C::KW / 8) + c;
+          const int j = i * (C::PW / 4) + c;                  // chunk of this thread in the step
           uint4 xb[NB];
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
-            const int m = nb * 8 + g;
-            if (m < M && kin) {
-              if constexpr (ACT == ACT_F16) {
-                xb[nb] = *reinterpret_cast<const uint4*>(xs + (size_t)m * rs + C::swz(chunk) * 16);
-              } else {
-                const uint2 raw = *reinterpret_cast<const uint2*>(xs + (size_t)m * rs + 8 * chunk);
-                cvt_i8x4_f16(raw.x, xb[nb].x, xb[nb].y);
-                cvt_i8x4_f16(raw.y, xb[nb].z, xb[nb].w);
-              }
+            const uint32_t o = (sbase + xoff[j]) & (kin ? xmask[nb] : 0u);
+            if constexpr (ACT == ACT_F16) {
+              xb[nb] = *reinterpret_cast<const uint4*>(xrow[nb] + o);
             } else {
-              xb[nb] = make_uint4(0, 0, 0, 0);
+              const uint2 raw = *reinterpret_cast<const uint2*>(xrow[nb] + o);
+              cvt_i8x4_f16(raw.x, xb[nb].x, xb[nb].y);
+              cvt_i8x4_f16(raw.y, xb[nb].z, xb[nb].w);
             }
           }
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
-            mma_16816(d[nb], ha[4 * c + 0], hb[4 * c + 0], ha[4 * c + 1], hb[4 * c + 1], xb[nb].x, xb[nb].y);
-            mma_16816(d[nb], ha[4 * c + 2], hb[4 * c + 2], ha[4 * c + 3], hb[4 * c + 3], xb[nb].z, xb[nb].w);
+            float (&dd)[4] = d[i & 1][nb];
+            mma_16816(dd, ha[4 * c + 0], hb[4 * c + 0], ha[4 * c + 1], hb[4 * c + 1], xb[nb].x, xb[nb].y);
+            mma_16816(dd, ha[4 * c + 2], hb[4 * c + 2], ha[4 * c + 3], hb[4 * c + 3], xb[nb].z, xb[nb].w);
           }
         }
       }
     }
   }
 
-  // ---- reduce the warps' K shares, then the epilogue ----
+  // ---- reduce the chains and the warps' K shares, then the epilogue ----
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) red[warp][nb][i][lane] = d[nb][i];
+    for (int i = 0; i < 4; ++i) red[warp][nb][i][lane] = d[0][nb][i] + d[1][nb][i];
   __syncthreads();
   if (warp < NB) {
     const int nb = warp;
@@ -207,9 +228,192 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
   }
 }
 
+// ---------------------------------------------------------------------------
+// Bulk-copy variant (the common case: 16 rows of packed weights fit in shared
+// memory).  One thread arms an mbarrier with the block's byte count and 16
+// lanes each issue one cp.async.bulk of a whole weight row, so ~32 KB per
+// block are in flight with no registers held; the warps then read 16-byte
+// pieces from padded rows (conflict-free) and proceed as above.
+// ---------------------------------------------------------------------------
+constexpr int WROW_PAD = 64;     // bytes between staged weight rows
+
+template <int BBITS, int ACT>
+__host__ __device__ constexpr int gemv_bulk_smem(int M, int K) {
+  return 16 * (K * BBITS / 8 + WROW_PAD) + M * gemv_row_stride<BBITS, ACT>(K) + 16 + 16;
+}
+
+template <int BBITS, int ACT, int NB, bool INTER>
+__global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* __restrict__ act,
+                                                                    const uint8_t* __restrict__ w, int M, int N, int K,
+                                                                    const __half* __restrict__ row_scale,
+                                                                    const __half* __restrict__ col_scale, int epi,
+                                                                    void* __restrict__ out, uint64_t timeout_ns,
+                                                                    int* status) {
+  using C = GemvCfg<BBITS>;
+  __shared__ float red[GEMV_WARPS][NB][4][32];
+  __shared__ __align__(8) uint64_t wbar;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int rb = K * BBITS / 8;                          // packed bytes per weight row
+  const int ws = rb + WROW_PAD;
+  uint8_t* const wsm = smem;                             // 16 staged weight rows
+  uint8_t* const xs = smem + 16 * ws;                    // M staged activation rows
+  const int rs = gemv_row_stride<BBITS, ACT>(K);
+  uint8_t* const zero_chunk = xs + (size_t)M * rs;
+  const int n0 = blockIdx.x * 16;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&wbar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&wbar, 16u * (uint32_t)rb);
+    __syncwarp();
+    if (threadIdx.x < 16) bulk_load(wsm + threadIdx.x * ws, w + (size_t)(n0 + threadIdx.x) * rb, (uint32_t)rb, &wbar);
+  }
+
+  // ---- stage the activations asynchronously ----
+  const int chunks_per_row = K >> 3;
+  if constexpr (ACT == ACT_F16) {
+    for (int idx = threadIdx.x; idx < M * chunks_per_row; idx += blockDim.x) {
+      const int m = idx / chunks_per_row, c = idx - m * chunks_per_row;
+      const int sstep = c / (C::STEP / 8), cin = c - sstep * (C::STEP / 8);
+      const int pos = C::chunk_pos(cin / C::CPT, cin % C::CPT);
+      cp_async_16(xs + (size_t)m * rs + (size_t)sstep * (C::STEP * 2) + pos * 16,
+                  static_cast<const __half*>(act) + (size_t)m * K + 8 * c);
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < M * chunks_per_row; idx += blockDim.x) {
+      const int m = idx / chunks_per_row, c = idx - m * chunks_per_row;
+      cp_async_8(xs + (size_t)m * rs + 8 * c, static_cast<const int8_t*>(act) + (size_t)m * K + 8 * c);
+    }
+  }
+  if (threadIdx.x == 0) *reinterpret_cast<uint4*>(zero_chunk) = make_uint4(0, 0, 0, 0);
+  cp_async_wait_all();
+  // Every thread waits for the weight rows; on a timeout the block still
+  // waits (bounded) for its copies before it may exit, and skips the math.
+  const bool w_ok = mbar_wait(&wbar, 0, timeout_ns, status);
+  if (!w_ok) mbar_wait(&wbar, 0, 4000000000ull, status);
+  __syncthreads();
+  const bool ok = __syncthreads_and(w_ok ? 1 : 0) != 0;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int nsteps = (K + C::STEP - 1) / C::STEP;
+  const int s_begin = (warp * nsteps) / GEMV_WARPS;
+  const int s_end = ok ? ((warp + 1) * nsteps) / GEMV_WARPS : s_begin;
+  const uint8_t* wr0 = wsm + g * ws + 16 * t;
+  const uint8_t* wr1 = wr0 + 8 * ws;
+
+  const uint8_t* xrow[NB];
+  uint32_t xmask[NB];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    const int m = nb * 8 + g;
+    xrow[nb] = m < M ? xs + (size_t)m * rs : zero_chunk;
+    xmask[nb] = m < M ? 0xffffffffu : 0u;
+  }
+  uint32_t xoff[C::CPT];
+#pragma unroll
+  for (int j = 0; j < C::CPT; ++j)
+    xoff[j] = ACT == ACT_F16 ? (uint32_t)(C::chunk_pos(t, j) * 16) : (uint32_t)((t * C::CPT + j) * 8);
+  constexpr uint32_t STEP_BYTES = ACT == ACT_F16 ? C::STEP * 2 : C::STEP;
+
+  float d[2][NB][4];
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[a][nb][i] = 0.0f;
+
+#pragma unroll 2
+  for (int s = s_begin; s < s_end; ++s) {
+    const bool kin = (s * C::STEP + t * C::E16) < K;
+    const uint32_t woff = (uint32_t)s * (C::STEP * BBITS / 8);
+    const uint4 va = kin ? *reinterpret_cast<const uint4*>(wr0 + woff) : make_uint4(0, 0, 0, 0);
+    const uint4 vb = kin ? *reinterpret_cast<const uint4*>(wr1 + woff) : make_uint4(0, 0, 0, 0);
+    const uint32_t sbase = (uint32_t)s * STEP_BYTES;
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+    const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t ha[C::PW], hb[C::PW];
+      convert_word<BBITS, INTER>(wa[i], ha);
+      convert_word<BBITS, INTER>(wb[i], hb);
+#pragma unroll
+      for (int c = 0; c < C::PW / 4; ++c) {
+        const int j = i * (C::PW / 4) + c;
+        uint4 xb[NB];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const uint32_t o = (sbase + xoff[j]) & (kin ? xmask[nb] : 0u);
+          if constexpr (ACT == ACT_F16) {
+            xb[nb] = *reinterpret_cast<const uint4*>(xrow[nb] + o);
+          } else {
+            const uint2 raw = *reinterpret_cast<const uint2*>(xrow[nb] + o);
+            cvt_i8x4_f16(raw.x, xb[nb].x, xb[nb].y);
+            cvt_i8x4_f16(raw.y, xb[nb].z, xb[nb].w);
+          }
+        }
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          float (&dd)[4] = d[i & 1][nb];
+          mma_16816(dd, ha[4 * c + 0], hb[4 * c + 0], ha[4 * c + 1], hb[4 * c + 1], xb[nb].x, xb[nb].y);
+          mma_16816(dd, ha[4 * c + 2], hb[4 * c + 2], ha[4 * c + 3], hb[4 * c + 3], xb[nb].z, xb[nb].w);
+        }
+      }
+    }
+  }
+
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red[warp][nb][i][lane] = d[0][nb][i] + d[1][nb][i];
+  __syncthreads();
+  if (warp < NB && ok) {
+    const int nb = warp;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int ww = 0; ww < GEMV_WARPS; ++ww) acc += red[ww][nb][i][lane];
+      const int n = n0 + g + (i >= 2 ? 8 : 0);
+      const int m = nb * 8 + 2 * t + (i & 1);
+      if (m >= M) continue;
+      const size_t o = (size_t)m * N + n;
+      if (epi == EPI_I32) {
+        static_cast<int32_t*>(out)[o] = __float2int_rn(acc);
+      } else {
+        float v = __fmul_rn(acc, __half2float(col_scale[n]));
+        if (epi == EPI_F16_ROWCOL) v = __fmul_rn(v, __half2float(row_scale[m]));
+        static_cast<__half*>(out)[o] = __float2half_rn(v);
+      }
+    }
+  }
+}
+
+template <int BBITS, int ACT, int NB, bool INTER>
+cudaError_t launch_bulk(const GemmArgs& g, cudaStream_t stream) {
+  int* status = nullptr;
+  cudaError_t e = device_status_ptr(&status);
+  if (e != cudaSuccess) return e;
+  const int smem = gemv_bulk_smem<BBITS, ACT>((int)g.M, (int)g.K);
+  auto kern = gemv_bulk_kernel<BBITS, ACT, NB, INTER>;
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<(unsigned)(g.N / 16), GEMV_WARPS * 32, smem, stream>>>(
+      g.a, static_cast<const uint8_t*>(g.b), (int)g.M, (int)g.N, (int)g.K,
+      reinterpret_cast<const __half*>(g.row_scale), reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c,
+      (uint64_t)wait_timeout_ns(), status);
+  return cudaGetLastError();
+}
+
 template <int BBITS, int ACT, int NB, bool INTER>
 cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
-  const int smem = (int)g.M * gemv_row_stride<BBITS, ACT>((int)g.K);
+  const int smem = (int)g.M * gemv_row_stride<BBITS, ACT>((int)g.K) + 16;
   auto kern = gemv_mma_kernel<BBITS, ACT, NB, INTER>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -224,6 +428,11 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
 template <int BBITS, int ACT>
 cudaError_t launch_bits_act(const GemmArgs& g, cudaStream_t stream) {
   const bool inter = g.layout == BQ_LAYOUT_INTERLEAVED;
+  if (gemv_bulk_smem<BBITS, ACT>((int)g.M, (int)g.K) <= 64 * 1024) {
+    if (g.M <= 8)
+      return inter ? launch_bulk<BBITS, ACT, 1, true>(g, stream) : launch_bulk<BBITS, ACT, 1, false>(g, stream);
+    return inter ? launch_bulk<BBITS, ACT, 2, true>(g, stream) : launch_bulk<BBITS, ACT, 2, false>(g, stream);
+  }
   if (g.M <= 8) return inter ? launch_t<BBITS, ACT, 1, true>(g, stream) : launch_t<BBITS, ACT, 1, false>(g, stream);
   return inter ? launch_t<BBITS, ACT, 2, true>(g, stream) : launch_t<BBITS, ACT, 2, false>(g, stream);
 }
@@ -231,7 +440,7 @@ cudaError_t launch_bits_act(const GemmArgs& g, cudaStream_t stream) {
 }  // namespace
 
 bool gemv_fits(int64_t M, int64_t K, int bbits) {
-  const int64_t bytes = M * (2 * K + (bbits == 4 ? 16 : 64));
+  const int64_t bytes = M * (2 * K + (bbits == 4 ? 16 : 64)) + 16;
   return M >= 1 && M <= 16 && bytes <= 200 * 1024;
 }
 
