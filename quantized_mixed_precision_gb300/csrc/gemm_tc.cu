@@ -93,7 +93,7 @@ constexpr int TC_NG = 1;
 
 // NG converter groups take the k-blocks in turn (group g converts k-blocks
 // kb = g (mod NG)), so conversion of consecutive k-blocks overlaps.
-template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST, int NG>
+template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST, int NG, int MINB = 1>
 struct Cfg {
   static constexpr int A_WARPS = AMODE == A_I8_TMEM ? 4 * NG : 0;
   static constexpr int B_WARPS = 8 * NG;
@@ -117,8 +117,8 @@ struct Cfg {
   static constexpr int OFF_RAW = ST * STAGE;
   static constexpr int OFF_BAR = OFF_RAW + RST * RSTAGE;
   static constexpr size_t SMEM = (size_t)OFF_BAR + 256 + 1024;
-  static_assert(USED_COLS <= 512, "tensor memory budget");
-  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(USED_COLS <= 512 / MINB, "tensor memory budget (MINB CTAs per SM)");
+  static_assert(MINB * (SMEM + 1024) <= 233472 && SMEM <= 232448, "shared memory budget");
   static_assert(STAGE % 1024 == 0 && RSTAGE % 1024 == 0, "stage alignment");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert((BN / (2 * NG)) % 32 == 0, "epilogue column parts are whole 32-column chunks");
@@ -166,12 +166,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, timeout_ns, status));
 }
 
-template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST, int NG>
-__global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG>::THREADS, 1)
+template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST, int NG, int MINB>
+__global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>::THREADS, MINB)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
                    int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
                    void* __restrict__ out, uint64_t timeout_ns, int* status) {
-  using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG>;
+  using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);   // MMA stage ready
@@ -439,9 +439,9 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST, int NG>
+template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST, int NG, int MINB>
 cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
-  using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG>;
+  using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>;
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
@@ -454,7 +454,7 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_RAW_ROW, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_tc_kernel<AMODE, BBITS, BN, NACC, INTER, ST, RST, NG>;
+  auto kern = gemm_tc_kernel<AMODE, BBITS, BN, NACC, INTER, ST, RST, NG, MINB>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
@@ -465,11 +465,11 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST, int NG = TC_NG>
+template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST, int NG = TC_NG, int MINB = 1>
 cudaError_t launch_layout(const GemmArgs& g, cudaStream_t stream) {
   if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN)
-    return launch_t<AMODE, BBITS, BN, NACC, false, ST, RST, NG>(g, stream);
-  return launch_t<AMODE, BBITS, BN, NACC, true, ST, RST, NG>(g, stream);
+    return launch_t<AMODE, BBITS, BN, NACC, false, ST, RST, NG, MINB>(g, stream);
+  return launch_t<AMODE, BBITS, BN, NACC, true, ST, RST, NG, MINB>(g, stream);
 }
 
 }  // namespace
