@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
   __shared__ float red[GEMV_WARPS][NB][4][32];
   extern __shared__ __align__(16) uint8_t xs[];       // M staged activation rows, then 16 zero bytes
   const int rs = gemv_row_stride<BBITS, ACT>(K);
-  uint8_t* const zero_chunk = xs + (size_t)M * rs;
+  // 16 zero bytes after the rows, 16-byte aligned (int8 rows have an 8-byte stride)
+  uint8_t* const zero_chunk = xs + (((size_t)M * rs + 15) & ~(size_t)15);
 
   // ---- stage the activations asynchronously (they are small and L2 resident) ----
   const int chunks_per_row = K >> 3;
@@ -180,11 +181,11 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
           uint4 xb[NB];
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
-            const uint32_t o = (sbase + xoff[j]) & (kin ? xmask[nb] : 0u);
+            const uint8_t* p = kin ? xrow[nb] + ((sbase + xoff[j]) & xmask[nb]) : zero_chunk;
             if constexpr (ACT == ACT_F16) {
-              xb[nb] = *reinterpret_cast<const uint4*>(xrow[nb] + o);
+              xb[nb] = *reinterpret_cast<const uint4*>(p);
             } else {
-              const uint2 raw = *reinterpret_cast<const uint2*>(xrow[nb] + o);
+              const uint2 raw = *reinterpret_cast<const uint2*>(p);
               cvt_i8x4_f16(raw.x, xb[nb].x, xb[nb].y);
               cvt_i8x4_f16(raw.y, xb[nb].z, xb[nb].w);
             }
@@ -239,7 +240,7 @@ constexpr int WROW_PAD = 64;     // bytes between staged weight rows
 
 template <int BBITS, int ACT>
 __host__ __device__ constexpr int gemv_bulk_smem(int M, int K) {
-  return 16 * (K * BBITS / 8 + WROW_PAD) + M * gemv_row_stride<BBITS, ACT>(K) + 16 + 16;
+  return 16 * (K * BBITS / 8 + WROW_PAD) + ((M * gemv_row_stride<BBITS, ACT>(K) + 15) & ~15) + 16;
 }
 
 template <int BBITS, int ACT, int NB, bool INTER>
@@ -258,7 +259,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   uint8_t* const wsm = smem;                             // 16 staged weight rows
   uint8_t* const xs = smem + 16 * ws;                    // M staged activation rows
   const int rs = gemv_row_stride<BBITS, ACT>(K);
-  uint8_t* const zero_chunk = xs + (size_t)M * rs;
+  // 16 zero bytes after the rows, 16-byte aligned (int8 rows have an 8-byte stride)
+  uint8_t* const zero_chunk = xs + (((size_t)M * rs + 15) & ~(size_t)15);
   const int n0 = blockIdx.x * 16;
 
   if (threadIdx.x == 0) {
@@ -347,11 +349,11 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
         uint4 xb[NB];
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          const uint32_t o = (sbase + xoff[j]) & (kin ? xmask[nb] : 0u);
+          const uint8_t* p = kin ? xrow[nb] + ((sbase + xoff[j]) & xmask[nb]) : zero_chunk;
           if constexpr (ACT == ACT_F16) {
-            xb[nb] = *reinterpret_cast<const uint4*>(xrow[nb] + o);
+            xb[nb] = *reinterpret_cast<const uint4*>(p);
           } else {
-            const uint2 raw = *reinterpret_cast<const uint2*>(xrow[nb] + o);
+            const uint2 raw = *reinterpret_cast<const uint2*>(p);
             cvt_i8x4_f16(raw.x, xb[nb].x, xb[nb].y);
             cvt_i8x4_f16(raw.y, xb[nb].z, xb[nb].w);
           }
@@ -413,7 +415,7 @@ cudaError_t launch_bulk(const GemmArgs& g, cudaStream_t stream) {
 
 template <int BBITS, int ACT, int NB, bool INTER>
 cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
-  const int smem = (int)g.M * gemv_row_stride<BBITS, ACT>((int)g.K) + 16;
+  const int smem = (((int)g.M * gemv_row_stride<BBITS, ACT>((int)g.K) + 15) & ~15) + 16;
   auto kern = gemv_mma_kernel<BBITS, ACT, NB, INTER>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -440,7 +442,7 @@ cudaError_t launch_bits_act(const GemmArgs& g, cudaStream_t stream) {
 }  // namespace
 
 bool gemv_fits(int64_t M, int64_t K, int bbits) {
-  const int64_t bytes = M * (2 * K + (bbits == 4 ? 16 : 64)) + 16;
+  const int64_t bytes = M * (2 * K + (bbits == 4 ? 16 : 64)) + 32;
   return M >= 1 && M <= 16 && bytes <= 200 * 1024;
 }
 
