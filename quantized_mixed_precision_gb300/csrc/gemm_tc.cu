@@ -19,10 +19,11 @@
 //
 // One 128 x BN output tile per CTA; warp roles:
 //   producer warp  one thread issues 2-D TMA loads (cp.async.bulk.tensor) of
-//                  the raw k-blocks of B (and of A) into a ring of RST raw
-//                  stages; rows past M / N arrive zero-filled.
+//                  the raw codes of B (and of A) into a ring of RST raw stages
+//                  of RKB k-blocks each (128-byte box rows, swizzled); rows
+//                  past M / N and columns past K arrive zero-filled.
 //   A warps (4/group) int8 activations only: thread = tile row = TMEM lane; reads
-//                  its 64 raw codes (64B-swizzled, conflict-free), converts
+//                  its 64 raw codes (128B-swizzled, conflict-free), converts
 //                  them to 32 fp16 pairs and writes them with tcgen05.st into
 //                  a TMEM stage that the MMA reads as its A operand.
 //                  fp16 activations need no conversion: the producer loads
@@ -100,12 +101,18 @@ struct Cfg {
   static constexpr int MMA_WARP = A_WARPS + B_WARPS;
   static constexpr int PRODUCER_WARP = MMA_WARP + 1;
   static constexpr int THREADS = (PRODUCER_WARP + 1) * 32;
+  // A raw stage holds RKB k-blocks, so every TMA box row is 128 bytes (64
+  // for 2-bit weights): the TMA engine moves a box row by row, and narrow
+  // rows waste its request rate.
+  static constexpr int RKB = BBITS == 8 ? 2 : 4;
   static constexpr int B_RAW_ROW = BK * BBITS / 8;            // raw weight bytes per row per k-block
-  static constexpr int B_PIECES_ROW = B_RAW_ROW / 16;
+  static constexpr int B_BOX_X = RKB * B_RAW_ROW;             // bytes per raw weight box row (128 or 64)
+  static constexpr int B_PIECES_ROW = B_RAW_ROW / 16;         // 16-byte pieces per row per k-block
   static constexpr int B_PIECES = BN * B_PIECES_ROW;
   static constexpr int NPB = (B_PIECES + B_THREADS - 1) / B_THREADS;
-  static constexpr int B_RAW = BN * B_RAW_ROW;
-  static constexpr int A_RAW = AMODE == A_I8_TMEM ? BM * BK : 0;   // int8 raw A per k-block
+  static constexpr int B_RAW = BN * B_BOX_X;                  // raw weight bytes per raw stage
+  static constexpr int A_BOX = BM * 128;                      // one int8 A box: 2 k-blocks x 128 rows
+  static constexpr int A_RAW = AMODE == A_I8_TMEM ? A_BOX * (RKB / 2) : 0;   // int8 raw A per raw stage
   static constexpr int A_TILE = AMODE == A_F16_SMEM ? BM * 128 : 0; // fp16 A tile in the MMA stage
   static constexpr int B_TILE = BN * 128;
   static constexpr int STAGE = A_TILE + B_TILE;
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
     }
     for (int s = 0; s < RST; ++s) {
       mbar_init(&rfull_bar[s], 1);
-      mbar_init(&rempty_bar[s], CONSUMERS);
+      mbar_init(&rempty_bar[s], CONSUMERS * NG);   // every group releases each raw stage once
     }
     mbar_init(accum_bar, 1);
     mbar_fence_init();
@@ -218,30 +225,35 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
+      int issued_groups = 0, issued_kb = 0;
       for (int kb = 0; kb < nkb; ++kb) {
-        const int rs = kb % RST;
-        if (!mbar_wait(&rempty_bar[rs], ((kb / RST) & 1) ^ 1, timeout_ns, status)) break;
-        uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE;
+        if (kb % C::RKB == 0) {
+          // raw stage for k-blocks [kb, kb + RKB): boxes past K read as zero
+          const int grp = kb / C::RKB;
+          const int rs = grp % RST;
+          if (!mbar_wait(&rempty_bar[rs], ((grp / RST) & 1) ^ 1, timeout_ns, status)) break;
+          uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE;
+          mbar_arrive_expect_tx(&rfull_bar[rs], C::A_RAW + C::B_RAW);
+          if constexpr (AMODE == A_I8_TMEM) {
+#pragma unroll
+            for (int b = 0; b < C::RKB / 2; ++b) tma_load_2d(raw + b * C::A_BOX, &tmap_a, (kb + 2 * b) * BK, m0, &rfull_bar[rs]);
+          }
+          tma_load_2d(raw + C::A_RAW, &tmap_b, kb * C::B_RAW_ROW, n0, &rfull_bar[rs]);
+          issued_groups = grp + 1;
+        }
         if constexpr (AMODE == A_F16_SMEM) {
           const int s = kb % ST;
           if (!mbar_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) break;
           mbar_arrive_expect_tx(&full_bar[s], BM * BK * 2);
           tma_load_2d(smem + s * C::STAGE, &tmap_a, kb * BK, m0, &full_bar[s]);
-          mbar_arrive_expect_tx(&rfull_bar[rs], C::B_RAW);
-          tma_load_2d(raw, &tmap_b, kb * C::B_RAW_ROW, n0, &rfull_bar[rs]);
-        } else {
-          mbar_arrive_expect_tx(&rfull_bar[rs], C::A_RAW + C::B_RAW);
-          tma_load_2d(raw, &tmap_a, kb * BK, m0, &rfull_bar[rs]);
-          tma_load_2d(raw + C::A_RAW, &tmap_b, kb * C::B_RAW_ROW, n0, &rfull_bar[rs]);
         }
-        issued = kb + 1;
+        issued_kb = kb + 1;
       }
       // no TMA write may land after the CTA has exited
-      for (int kb = issued > RST ? issued - RST : 0; kb < issued; ++kb)
-        mbar_wait(&rfull_bar[kb % RST], (kb / RST) & 1, DRAIN_TIMEOUT_NS, status);
+      for (int grp = issued_groups > RST ? issued_groups - RST : 0; grp < issued_groups; ++grp)
+        mbar_wait(&rfull_bar[grp % RST], (grp / RST) & 1, DRAIN_TIMEOUT_NS, status);
       if constexpr (AMODE == A_F16_SMEM) {
-        for (int kb = issued > ST ? issued - ST : 0; kb < issued; ++kb)
+        for (int kb = issued_kb > ST ? issued_kb - ST : 0; kb < issued_kb; ++kb)
           mbar_wait(&full_bar[kb % ST], (kb / ST) & 1, DRAIN_TIMEOUT_NS, status);
       }
     }
@@ -282,14 +294,15 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
     const int q = warp & 3;                               // TMEM lane quadrant
     const int r = q * 32 + lane;                          // tile row == TMEM lane
     for (int kb = warp >> 2; kb < nkb; kb += NG) {
-      const int rs = kb % RST;
-      if (!warp_wait(&rfull_bar[rs], (kb / RST) & 1, timeout_ns, status)) break;
-      const uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE;
+      const int grp = kb / C::RKB, rs = grp % RST;
+      if (!warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) break;
+      // this k-block is half of a 128-byte box row (128B swizzle: chunk c of row r at c ^ (r & 7))
+      const uint8_t* box = smem + C::OFF_RAW + rs * C::RSTAGE + ((kb % C::RKB) >> 1) * C::A_BOX + r * 128;
+      const int c0 = (kb & 1) * 4;
       uint4 v[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)   // 64B swizzle: chunk j of row r at j ^ ((r >> 1) & 3)
-        v[j] = *reinterpret_cast<const uint4*>(raw + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
-      mbar_arrive(&rempty_bar[rs]);
+      for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(box + (((c0 + j) ^ (r & 7)) << 4));
+      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
       uint32_t h[32];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -311,19 +324,25 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
     const int c = (bw & 7) * 32 + lane;                   // thread within its group
     bool ok = true;
     for (int kb = bw >> 3; kb < nkb; kb += NG) {
-      const int rs = kb % RST;
-      if (!warp_wait(&rfull_bar[rs], (kb / RST) & 1, timeout_ns, status)) {
+      const int grp = kb / C::RKB, rs = grp % RST;
+      if (!warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
         ok = false;
         break;
       }
       const uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE + C::A_RAW;
+      // piece pi is (row pi % BN, piece pi / BN): a quarter warp reads 8 rows,
+      // whose swizzled chunk positions differ (conflict-free)
       uint4 v[C::NPB];
 #pragma unroll
       for (int i = 0; i < C::NPB; ++i) {
         const int pi = c + i * B_THREADS;
-        v[i] = pi < C::B_PIECES ? *reinterpret_cast<const uint4*>(raw + pi * 16) : make_uint4(0, 0, 0, 0);
+        const int r = pi % BN, sub = pi / BN;
+        const int chunk = (kb % C::RKB) * C::B_PIECES_ROW + sub;
+        const int pos = C::B_BOX_X == 128 ? (chunk ^ (r & 7)) : (chunk ^ ((r >> 1) & 3));
+        v[i] = pi < C::B_PIECES ? *reinterpret_cast<const uint4*>(raw + r * C::B_BOX_X + (pos << 4))
+                                : make_uint4(0, 0, 0, 0);
       }
-      mbar_arrive(&rempty_bar[rs]);
+      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
       const int s = kb % ST;
       if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) {
         ok = false;
@@ -333,7 +352,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
 #pragma unroll
       for (int i = 0; i < C::NPB; ++i) {
         const int pi = c + i * B_THREADS;
-        if (pi < C::B_PIECES) convert_b_piece<BBITS, INTER>(tb, pi / C::B_PIECES_ROW, pi % C::B_PIECES_ROW, v[i]);
+        if (pi < C::B_PIECES) convert_b_piece<BBITS, INTER>(tb, pi % BN, pi / BN, v[i]);
       }
       fence_proxy_async_smem();
       mbar_arrive(&full_bar[s]);
@@ -449,10 +468,11 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
   if (AMODE == A_F16_SMEM) {
     e = make_map(&ma, g.a, 2, (uint64_t)g.K, (uint64_t)g.M, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
-    e = make_map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, BK, BM, CU_TENSOR_MAP_SWIZZLE_64B);
+    e = make_map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, 2 * BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (e != cudaSuccess) return e;
-  e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_RAW_ROW, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+  e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_BOX_X, BN,
+               C::B_BOX_X == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
   auto kern = gemm_tc_kernel<AMODE, BBITS, BN, NACC, INTER, ST, RST, NG, MINB>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
@@ -479,19 +499,19 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream) {
   if (g.act == ACT_I8 && g.bbits == 8) {
     if (g.epi == EPI_I32) {
       // int32 output: slices of at most 1024 k keep every partial sum < 2**24 exactly
-      if (nkb <= 16) return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 4>(g, stream);
-      if (nkb <= 32) return launch_layout<A_I8_TMEM, 8, 128, 2, 4, 4>(g, stream);
-      if (nkb <= 64) return launch_layout<A_I8_TMEM, 8, 64, 4, 4, 4, 1>(g, stream);
+      if (nkb <= 16) return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 2>(g, stream);
+      if (nkb <= 32) return launch_layout<A_I8_TMEM, 8, 128, 2, 4, 2>(g, stream);
+      if (nkb <= 64) return launch_layout<A_I8_TMEM, 8, 64, 4, 4, 2, 1>(g, stream);
       return cudaErrorInvalidValue;
     }
-    return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 4>(g, stream);
+    return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 2>(g, stream);
   }
   // int8 activations with 4- / 2-bit weights: every partial sum < 2**24 (host-bounded K)
-  if (g.act == ACT_I8 && g.bbits == 4) return launch_layout<A_I8_TMEM, 4, 256, 1, 4, 5>(g, stream);
-  if (g.act == ACT_I8 && g.bbits == 2) return launch_layout<A_I8_TMEM, 2, 256, 1, 4, 6>(g, stream);
+  if (g.act == ACT_I8 && g.bbits == 4) return launch_layout<A_I8_TMEM, 4, 256, 1, 3, 2>(g, stream);
+  if (g.act == ACT_I8 && g.bbits == 2) return launch_layout<A_I8_TMEM, 2, 256, 1, 4, 2>(g, stream);
   if (g.act == ACT_F16 && g.bbits == 4) {
-    if (nkb >= 2) return launch_layout<A_F16_SMEM, 4, 256, 2, 3, 8>(g, stream);
-    return launch_layout<A_F16_SMEM, 4, 256, 1, 3, 8>(g, stream);
+    if (nkb >= 2) return launch_layout<A_F16_SMEM, 4, 256, 2, 3, 2>(g, stream);
+    return launch_layout<A_F16_SMEM, 4, 256, 1, 3, 2>(g, stream);
   }
   return cudaErrorInvalidValue;
 }
