@@ -231,16 +231,38 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
 
 // ---------------------------------------------------------------------------
 // Bulk-copy variant (the common case: 16 rows of packed weights fit in shared
-// memory).  One thread arms an mbarrier with the block's byte count and 16
-// lanes each issue one cp.async.bulk of a whole weight row, so ~32 KB per
-// block are in flight with no registers held; the warps then read 16-byte
-// pieces from padded rows (conflict-free) and proceed as above.
+// memory).  Each warp owns a quarter of K and an mbarrier: its lane 0 arms
+// the barrier with the byte count and lanes 0-15 each issue one
+// cp.async.bulk of that quarter of one weight row, so the block keeps ~32 KB
+// in flight without holding registers and every warp starts as soon as its
+// own quarter has landed.  The activations (at most 16 rows) are read as
+// MMA fragments straight from global memory (L1 resident) at the start of
+// each step, so they never queue behind the weight stream.  The kernel
+// supports programmatic dependent launch: the weights (read-only) are
+// requested before griddepcontrol.wait, the activations are read and the
+// outputs written only after it, so a chain of layer GEMVs streams the next
+// layer's weights while the previous one finishes.
 // ---------------------------------------------------------------------------
 constexpr int WROW_PAD = 64;     // bytes between staged weight rows
 
-template <int BBITS, int ACT>
-__host__ __device__ constexpr int gemv_bulk_smem(int M, int K) {
-  return 16 * (K * BBITS / 8 + WROW_PAD) + ((M * gemv_row_stride<BBITS, ACT>(K) + 15) & ~15) + 16;
+template <int BBITS>
+__host__ __device__ constexpr int gemv_bulk_smem(int K) {
+  return 16 * (K * BBITS / 8 + WROW_PAD);
+}
+
+// 8 activation values (k0 .. k0+7) of row m as 4 fp16x2 words, or zeros.
+template <int ACT>
+__device__ __forceinline__ uint4 load_x8(const void* act, int m, int K, int k0, bool valid) {
+  if (!valid) return make_uint4(0, 0, 0, 0);
+  if constexpr (ACT == ACT_F16) {
+    return __ldg(reinterpret_cast<const uint4*>(static_cast<const __half*>(act) + (size_t)m * K + k0));
+  } else {
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const int8_t*>(act) + (size_t)m * K + k0));
+    uint4 v;
+    cvt_i8x4_f16(raw.x, v.x, v.y);
+    cvt_i8x4_f16(raw.y, v.z, v.w);
+    return v;
+  }
 }
 
 template <int BBITS, int ACT, int NB, bool INTER>
@@ -252,74 +274,49 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
                                                                     int* status) {
   using C = GemvCfg<BBITS>;
   __shared__ float red[GEMV_WARPS][NB][4][32];
-  __shared__ __align__(8) uint64_t wbar;
-  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ __align__(8) uint64_t wbar[GEMV_WARPS];
+  extern __shared__ __align__(16) uint8_t wsm[];         // 16 staged weight rows
   const int rb = K * BBITS / 8;                          // packed bytes per weight row
   const int ws = rb + WROW_PAD;
-  uint8_t* const wsm = smem;                             // 16 staged weight rows
-  uint8_t* const xs = smem + 16 * ws;                    // M staged activation rows
-  const int rs = gemv_row_stride<BBITS, ACT>(K);
-  // 16 zero bytes after the rows, 16-byte aligned (int8 rows have an 8-byte stride)
-  uint8_t* const zero_chunk = xs + (((size_t)M * rs + 15) & ~(size_t)15);
   const int n0 = blockIdx.x * 16;
-
-  if (threadIdx.x == 0) {
-    mbar_init(&wbar, 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(&wbar, 16u * (uint32_t)rb);
-    __syncwarp();
-    if (threadIdx.x < 16) bulk_load(wsm + threadIdx.x * ws, w + (size_t)(n0 + threadIdx.x) * rb, (uint32_t)rb, &wbar);
-  }
-
-  // ---- stage the activations asynchronously ----
-  const int chunks_per_row = K >> 3;
-  if constexpr (ACT == ACT_F16) {
-    for (int idx = threadIdx.x; idx < M * chunks_per_row; idx += blockDim.x) {
-      const int m = idx / chunks_per_row, c = idx - m * chunks_per_row;
-      const int sstep = c / (C::STEP / 8), cin = c - sstep * (C::STEP / 8);
-      const int pos = C::chunk_pos(cin / C::CPT, cin % C::CPT);
-      cp_async_16(xs + (size_t)m * rs + (size_t)sstep * (C::STEP * 2) + pos * 16,
-                  static_cast<const __half*>(act) + (size_t)m * K + 8 * c);
-    }
-  } else {
-    for (int idx = threadIdx.x; idx < M * chunks_per_row; idx += blockDim.x) {
-      const int m = idx / chunks_per_row, c = idx - m * chunks_per_row;
-      cp_async_8(xs + (size_t)m * rs + 8 * c, static_cast<const int8_t*>(act) + (size_t)m * K + 8 * c);
-    }
-  }
-  if (threadIdx.x == 0) *reinterpret_cast<uint4*>(zero_chunk) = make_uint4(0, 0, 0, 0);
-  cp_async_wait_all();
-  // Every thread waits for the weight rows; on a timeout the block still
-  // waits (bounded) for its copies before it may exit, and skips the math.
-  const bool w_ok = mbar_wait(&wbar, 0, timeout_ns, status);
-  if (!w_ok) mbar_wait(&wbar, 0, 4000000000ull, status);
-  __syncthreads();
-  const bool ok = __syncthreads_and(w_ok ? 1 : 0) != 0;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
   const int nsteps = (K + C::STEP - 1) / C::STEP;
   const int s_begin = (warp * nsteps) / GEMV_WARPS;
-  const int s_end = ok ? ((warp + 1) * nsteps) / GEMV_WARPS : s_begin;
+  const int s_end = ((warp + 1) * nsteps) / GEMV_WARPS;
+  constexpr int STEP_W = C::STEP * BBITS / 8;            // packed bytes of one step (64)
+  const int seg_off = s_begin * STEP_W;
+  const int seg = min((s_end - s_begin) * STEP_W, rb - seg_off);   // this warp's bytes per row
+
+  if (lane == 0) {
+    mbar_init(&wbar[warp], 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  // ---- weights first (read-only, independent of any earlier kernel) ----
+  if (seg > 0) {
+    if (lane == 0) mbar_arrive_expect_tx(&wbar[warp], 16u * (uint32_t)seg);
+    __syncwarp();
+    if (lane < 16)
+      bulk_load(wsm + lane * ws + seg_off, w + (size_t)(n0 + lane) * rb + seg_off, (uint32_t)seg, &wbar[warp]);
+  }
+  // let a dependent kernel start its own weight prefetch; then wait for the
+  // kernel that produced the activations before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // Each warp waits for its own quarter; on a timeout it still waits
+  // (bounded) for its copies before it may exit, and skips the math.
+  bool w_ok = true;
+  if (seg > 0) {
+    w_ok = mbar_wait(&wbar[warp], 0, timeout_ns, status);
+    if (!w_ok) mbar_wait(&wbar[warp], 0, 4000000000ull, status);
+  }
+  w_ok = __all_sync(0xffffffffu, w_ok);
+
+  const int g = lane >> 2, t = lane & 3;
+  const int s_stop = w_ok ? s_end : s_begin;
   const uint8_t* wr0 = wsm + g * ws + 16 * t;
   const uint8_t* wr1 = wr0 + 8 * ws;
-
-  const uint8_t* xrow[NB];
-  uint32_t xmask[NB];
-#pragma unroll
-  for (int nb = 0; nb < NB; ++nb) {
-    const int m = nb * 8 + g;
-    xrow[nb] = m < M ? xs + (size_t)m * rs : zero_chunk;
-    xmask[nb] = m < M ? 0xffffffffu : 0u;
-  }
-  uint32_t xoff[C::CPT];
-#pragma unroll
-  for (int j = 0; j < C::CPT; ++j)
-    xoff[j] = ACT == ACT_F16 ? (uint32_t)(C::chunk_pos(t, j) * 16) : (uint32_t)((t * C::CPT + j) * 8);
-  constexpr uint32_t STEP_BYTES = ACT == ACT_F16 ? C::STEP * 2 : C::STEP;
 
   float d[2][NB][4];
 #pragma unroll
@@ -330,12 +327,18 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
       for (int i = 0; i < 4; ++i) d[a][nb][i] = 0.0f;
 
 #pragma unroll 2
-  for (int s = s_begin; s < s_end; ++s) {
-    const bool kin = (s * C::STEP + t * C::E16) < K;
-    const uint32_t woff = (uint32_t)s * (C::STEP * BBITS / 8);
+  for (int s = s_begin; s < s_stop; ++s) {
+    const int kbase = s * C::STEP + t * C::E16;          // first k of this thread's 16 bytes
+    const bool kin = kbase < K;
+    // activation fragments first (L1/L2 resident), overlapping the conversion
+    uint4 xb[C::CPT][NB];
+#pragma unroll
+    for (int j = 0; j < C::CPT; ++j)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = load_x8<ACT>(act, nb * 8 + g, K, kbase + 8 * j, kin && nb * 8 + g < M);
+    const uint32_t woff = (uint32_t)s * STEP_W;
     const uint4 va = kin ? *reinterpret_cast<const uint4*>(wr0 + woff) : make_uint4(0, 0, 0, 0);
     const uint4 vb = kin ? *reinterpret_cast<const uint4*>(wr1 + woff) : make_uint4(0, 0, 0, 0);
-    const uint32_t sbase = (uint32_t)s * STEP_BYTES;
     const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
     const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
@@ -346,23 +349,11 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
 #pragma unroll
       for (int c = 0; c < C::PW / 4; ++c) {
         const int j = i * (C::PW / 4) + c;
-        uint4 xb[NB];
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const uint8_t* p = kin ? xrow[nb] + ((sbase + xoff[j]) & xmask[nb]) : zero_chunk;
-          if constexpr (ACT == ACT_F16) {
-            xb[nb] = *reinterpret_cast<const uint4*>(p);
-          } else {
-            const uint2 raw = *reinterpret_cast<const uint2*>(p);
-            cvt_i8x4_f16(raw.x, xb[nb].x, xb[nb].y);
-            cvt_i8x4_f16(raw.y, xb[nb].z, xb[nb].w);
-          }
-        }
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
           float (&dd)[4] = d[i & 1][nb];
-          mma_16816(dd, ha[4 * c + 0], hb[4 * c + 0], ha[4 * c + 1], hb[4 * c + 1], xb[nb].x, xb[nb].y);
-          mma_16816(dd, ha[4 * c + 2], hb[4 * c + 2], ha[4 * c + 3], hb[4 * c + 3], xb[nb].z, xb[nb].w);
+          mma_16816(dd, ha[4 * c + 0], hb[4 * c + 0], ha[4 * c + 1], hb[4 * c + 1], xb[j][nb].x, xb[j][nb].y);
+          mma_16816(dd, ha[4 * c + 2], hb[4 * c + 2], ha[4 * c + 3], hb[4 * c + 3], xb[j][nb].z, xb[j][nb].w);
         }
       }
     }
@@ -372,7 +363,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
     for (int i = 0; i < 4; ++i) red[warp][nb][i][lane] = d[0][nb][i] + d[1][nb][i];
-  __syncthreads();
+  const bool ok = __syncthreads_and(w_ok ? 1 : 0) != 0;
   if (warp < NB && ok) {
     const int nb = warp;
 #pragma unroll
@@ -400,16 +391,32 @@ cudaError_t launch_bulk(const GemmArgs& g, cudaStream_t stream) {
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
-  const int smem = gemv_bulk_smem<BBITS, ACT>((int)g.M, (int)g.K);
+  const int smem = gemv_bulk_smem<BBITS>((int)g.K);
   auto kern = gemv_bulk_kernel<BBITS, ACT, NB, INTER>;
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<(unsigned)(g.N / 16), GEMV_WARPS * 32, smem, stream>>>(
-      g.a, static_cast<const uint8_t*>(g.b), (int)g.M, (int)g.N, (int)g.K,
-      reinterpret_cast<const __half*>(g.row_scale), reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c,
-      (uint64_t)wait_timeout_ns(), status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(g.N / 16));
+  cfg.blockDim = dim3(GEMV_WARPS * 32);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const void* a = g.a;
+  const uint8_t* b = static_cast<const uint8_t*>(g.b);
+  int M = (int)g.M, N = (int)g.N, K = (int)g.K;
+  const __half* rsc = reinterpret_cast<const __half*>(g.row_scale);
+  const __half* csc = reinterpret_cast<const __half*>(g.col_scale);
+  int epi = g.epi;
+  void* c = g.c;
+  uint64_t to = (uint64_t)wait_timeout_ns();
+  e = cudaLaunchKernelEx(&cfg, kern, a, b, M, N, K, rsc, csc, epi, c, to, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -430,7 +437,7 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
 template <int BBITS, int ACT>
 cudaError_t launch_bits_act(const GemmArgs& g, cudaStream_t stream) {
   const bool inter = g.layout == BQ_LAYOUT_INTERLEAVED;
-  if (gemv_bulk_smem<BBITS, ACT>((int)g.M, (int)g.K) <= 64 * 1024) {
+  if (gemv_bulk_smem<BBITS>((int)g.K) <= 64 * 1024) {
     if (g.M <= 8)
       return inter ? launch_bulk<BBITS, ACT, 1, true>(g, stream) : launch_bulk<BBITS, ACT, 1, false>(g, stream);
     return inter ? launch_bulk<BBITS, ACT, 2, true>(g, stream) : launch_bulk<BBITS, ACT, 2, false>(g, stream);
