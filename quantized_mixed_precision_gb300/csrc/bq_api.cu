@@ -62,6 +62,27 @@ bq_status run_gemm(GemmArgs g, void* stream) {
 
 int64_t wait_timeout_ns() { return g_wait_timeout_ns.load(); }
 
+cudaError_t set_smem_once_ptr(const void* kern, int bytes) {
+  struct Entry {
+    const void* kern;
+    int dev;
+    int bytes;
+  };
+  static Entry table[256];
+  static std::atomic<int> used{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int n = used.load();
+  for (int i = 0; i < n && i < 256; ++i)
+    if (table[i].kern == kern && table[i].dev == dev && table[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  const int slot = used.fetch_add(1);
+  if (slot < 256) table[slot] = Entry{kern, dev, bytes};
+  return cudaSuccess;
+}
+
 }  // namespace bq
 
 using namespace bq;

@@ -41,6 +41,15 @@ struct GemmArgs {
   void* c;                // int32 or fp16 (M, N)
 };
 
+// Raise a kernel's dynamic shared-memory limit once per (device, kernel), so
+// that later launches make no attribute call (e.g. inside a stream capture).
+cudaError_t set_smem_once_ptr(const void* kern, int bytes);
+
+template <typename Kernel>
+cudaError_t set_smem_once(Kernel kern, int bytes) {
+  return set_smem_once_ptr(reinterpret_cast<const void*>(kern), bytes);
+}
+
 // Skinny-M path (M <= 16): one pass over the weights, legacy mma.sync fp16.
 // gemv_fits tells whether its staged activations fit in shared memory.
 bool gemv_fits(int64_t M, int64_t K, int bbits);

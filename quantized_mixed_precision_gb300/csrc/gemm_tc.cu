@@ -475,7 +475,7 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
                C::B_BOX_X == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
   auto kern = gemm_tc_kernel<AMODE, BBITS, BN, NACC, INTER, ST, RST, NG, MINB>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(ma, mb, (int)g.M, (int)g.N, (int)g.K,

@@ -394,7 +394,7 @@ cudaError_t launch_bulk(const GemmArgs& g, cudaStream_t stream) {
   const int smem = gemv_bulk_smem<BBITS>((int)g.K);
   auto kern = gemv_bulk_kernel<BBITS, ACT, NB, INTER>;
   if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = set_smem_once(kern, smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -425,7 +425,7 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
   const int smem = (((int)g.M * gemv_row_stride<BBITS, ACT>((int)g.K) + 15) & ~15) + 16;
   auto kern = gemv_mma_kernel<BBITS, ACT, NB, INTER>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_smem_once(kern, smem);
     if (e != cudaSuccess) return e;
   }
   kern<<<(unsigned)(g.N / 16), GEMV_WARPS * 32, smem, stream>>>(
