@@ -186,13 +186,19 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
   uint64_t* rfull_bar = empty_bar + ST;                                  // raw stage landed
   uint64_t* rempty_bar = rfull_bar + RST;                                // raw stage read
   uint64_t* accum_bar = rempty_bar + RST;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
+  uint64_t* ready_bar = accum_bar + 1;                                   // split-K: peers' pipelines done
+  uint64_t* recv_bar = ready_bar + 1;                                    // split-K: peers' partials landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int m0 = blockIdx.y * BM;
   const int n0 = blockIdx.x * BN;
-  const int nkb = K / BK;
+  // Split-K: the gridDim.z CTAs of a cluster share one output tile and take
+  // consecutive ranges of k-blocks; kb below counts within this CTA's range.
+  const int S = gridDim.z;
+  const int kb_lo = (int)(((long long)blockIdx.z * (K / BK)) / S);
+  const int nkb = (int)(((long long)(blockIdx.z + 1) * (K / BK)) / S) - kb_lo;
   // threads that consume one k-block: one A group (4 warps) and one B group (8 warps)
   constexpr int CONSUMERS = (C::A_WARPS / NG + 8) * 32;
 
@@ -207,6 +213,8 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
       mbar_init(&rempty_bar[s], CONSUMERS * NG);   // every group releases each raw stage once
     }
     mbar_init(accum_bar, 1);
+    mbar_init(ready_bar, S > 1 ? S - 1 : 1);
+    mbar_init(recv_bar, S * B_THREADS);
     mbar_fence_init();
   }
   if (warp == C::MMA_WARP) {
@@ -221,6 +229,8 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // peers may arrive on this CTA's barriers only once they are initialised
+  if (S > 1) cluster_sync_all();
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer
@@ -236,16 +246,17 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
           mbar_arrive_expect_tx(&rfull_bar[rs], C::A_RAW + C::B_RAW);
           if constexpr (AMODE == A_I8_TMEM) {
 #pragma unroll
-            for (int b = 0; b < C::RKB / 2; ++b) tma_load_2d(raw + b * C::A_BOX, &tmap_a, (kb + 2 * b) * BK, m0, &rfull_bar[rs]);
+            for (int b = 0; b < C::RKB / 2; ++b)
+              tma_load_2d(raw + b * C::A_BOX, &tmap_a, (kb_lo + kb + 2 * b) * BK, m0, &rfull_bar[rs]);
           }
-          tma_load_2d(raw + C::A_RAW, &tmap_b, kb * C::B_RAW_ROW, n0, &rfull_bar[rs]);
+          tma_load_2d(raw + C::A_RAW, &tmap_b, (kb_lo + kb) * C::B_RAW_ROW, n0, &rfull_bar[rs]);
           issued_groups = grp + 1;
         }
         if constexpr (AMODE == A_F16_SMEM) {
           const int s = kb % ST;
           if (!mbar_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) break;
           mbar_arrive_expect_tx(&full_bar[s], BM * BK * 2);
-          tma_load_2d(smem + s * C::STAGE, &tmap_a, kb * BK, m0, &full_bar[s]);
+          tma_load_2d(smem + s * C::STAGE, &tmap_a, (kb_lo + kb) * BK, m0, &full_bar[s]);
         }
         issued_kb = kb + 1;
       }
@@ -359,7 +370,8 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
     }
 
     // ------------------------------------------------------------ epilogue
-    const bool acc_ok = warp_wait(accum_bar, 0, ok ? timeout_ns : 0, status);
+    // (with split-K the epilogue runs after the cluster reduction below)
+    const bool acc_ok = S == 1 && warp_wait(accum_bar, 0, ok ? timeout_ns : 0, status);
     tc_fence_after();
     if (acc_ok) {
       // 2 * NG warps share each TMEM lane quadrant; each takes a column part
@@ -419,6 +431,108 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
 
   tc_fence_before();
   __syncthreads();
+
+  if (S > 1) {
+    // ------------------------------------------------------------ split-K reduction
+    // Every CTA's pipeline is idle now (MMAs, TMA loads and converters are
+    // done), so its pipeline buffers become a receive area.  The tile's BN/32
+    // column chunks are owned round-robin (chunk c by CTA c % S); each CTA
+    // sends every chunk of its partial accumulator into its owner's area
+    // (distributed shared memory, slot [sender][c / S], rows 128B-swizzled),
+    // arrives on every CTA's receive barrier, and then reduces and stores the
+    // chunks it owns.  All handshakes are mbarriers with bounded waits.
+    if constexpr (NACC == 1) {   // split-K runs with one accumulator slice
+    constexpr int NCH = BN / 32;
+    const int rank = (int)cluster_ctarank();
+    const int slots = (NCH + S - 1) / S;
+    const uint32_t recv_base = smem_u32(smem);
+    if (tid == 0) {
+      for (int p = 0; p < S; ++p)
+        if (p != rank) mbar_arrive_cluster(mapa_shared(smem_u32(ready_bar), (uint32_t)p));
+    }
+    if (warp >= C::A_WARPS && warp < C::A_WARPS + 8) {
+      const int bw = warp - C::A_WARPS;
+      const int q = warp & 3, chalf = bw >> 2;
+      const int r = 32 * q + lane;                          // tile row (TMEM lane)
+      bool ok = __all_sync(0xffffffffu, mbar_wait(accum_bar, 0, DRAIN_TIMEOUT_NS, status));
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(ready_bar, 0, DRAIN_TIMEOUT_NS, status)) && ok;
+      tc_fence_after();
+      if (ok) {
+        for (int cc = 0; cc < NCH / 2; ++cc) {
+          const int c = chalf * (NCH / 2) + cc;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * c), v);
+          tmem_ld_wait();
+          const uint32_t owner = (uint32_t)(c % S);
+          const uint32_t row_addr = recv_base + (uint32_t)(((rank * slots + c / S) * BM + r) * 128);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_cluster_v4(mapa_shared(row_addr + (uint32_t)((j ^ (r & 7)) << 4), owner),
+                          make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        }
+      }
+      // one arrival per thread on every CTA's receive barrier (also on error,
+      // so no peer waits in vain)
+      for (int p = 0; p < S; ++p) mbar_arrive_cluster(mapa_shared(smem_u32(recv_bar), (uint32_t)p));
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(recv_bar, 0, DRAIN_TIMEOUT_NS, status)) && ok;
+      if (ok) {
+        const int row = m0 + r;
+        const bool row_ok = row < M;
+        float rsc = 1.0f;
+        if (epi == EPI_F16_ROWCOL && row_ok) rsc = __half2float(row_scale[row]);
+        const int owned = (NCH - rank + S - 1) / S;
+        for (int slot = chalf; slot < owned; slot += 2) {
+          const int c = rank + slot * S;
+          float acc[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+          for (int src = 0; src < S; ++src) {
+            const uint8_t* rowp = smem + ((src * slots + slot) * BM + r) * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint4 w4 = *reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4));
+              acc[4 * j] += __uint_as_float(w4.x);
+              acc[4 * j + 1] += __uint_as_float(w4.y);
+              acc[4 * j + 2] += __uint_as_float(w4.z);
+              acc[4 * j + 3] += __uint_as_float(w4.w);
+            }
+          }
+          const int ncol = n0 + 32 * c;
+          if (row_ok && ncol < N) {
+            if (epi == EPI_I32) {
+              int4* dst = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + (size_t)row * N + ncol);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_int4(__float2int_rn(acc[4 * i]), __float2int_rn(acc[4 * i + 1]),
+                                   __float2int_rn(acc[4 * i + 2]), __float2int_rn(acc[4 * i + 3]));
+            } else {
+              uint32_t hv[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const __half2 sc2 = *reinterpret_cast<const __half2*>(col_scale + ncol + 2 * i);
+                float x0 = __fmul_rn(acc[2 * i], __low2float(sc2));
+                float x1 = __fmul_rn(acc[2 * i + 1], __high2float(sc2));
+                if (epi == EPI_F16_ROWCOL) {
+                  x0 = __fmul_rn(x0, rsc);
+                  x1 = __fmul_rn(x1, rsc);
+                }
+                const __half2 h2 = __halves2half2(__float2half_rn(x0), __float2half_rn(x1));
+                hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(out) + (size_t)row * N + ncol);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+            }
+          }
+        }
+      }
+    }
+    }  // NACC == 1
+    tc_fence_before();
+    __syncthreads();
+  }
+
   if (warp == C::MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, C::NCOLS);
@@ -459,8 +573,10 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_
 }
 
 template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST, int NG, int MINB>
-cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
+cudaError_t launch_t(const GemmArgs& g, int split, cudaStream_t stream) {
   using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>;
+  // the split-K receive area (split x slots x 16 KB) must fit in the pipeline buffers
+  if (NACC != 1 || split < 1 || split * ((BN / 32 + split - 1) / split) * BM * 128 > C::OFF_BAR) split = 1;
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
@@ -477,19 +593,65 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
   auto kern = gemm_tc_kernel<AMODE, BBITS, BN, NACC, INTER, ST, RST, NG, MINB>;
   e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(ma, mb, (int)g.M, (int)g.N, (int)g.K,
-                                              reinterpret_cast<const __half*>(g.row_scale),
-                                              reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c,
-                                              (uint64_t)wait_timeout_ns(), status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM), (unsigned)split);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)split;
+  cfg.attrs = attr;
+  cfg.numAttrs = split > 1 ? 1 : 0;
+  const int M = (int)g.M, N = (int)g.N, K = (int)g.K;
+  const __half* rsc = reinterpret_cast<const __half*>(g.row_scale);
+  const __half* csc = reinterpret_cast<const __half*>(g.col_scale);
+  const int epi = g.epi;
+  void* out = g.c;
+  const uint64_t to = (uint64_t)wait_timeout_ns();
+  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, M, N, K, rsc, csc, epi, out, to, status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+int sm_count() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!n[dev] && cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n[dev] = 148;
+  return n[dev];
+}
+
+// Split-K factor for a grid of `tiles` output tiles of nkb k-blocks each:
+// minimise (waves of CTAs) x (k-blocks per CTA + a fixed per-CTA cost of about
+// 8 k-blocks for set-up, epilogue and the cluster reduction).  Only grids
+// smaller than one wave are split.
+int choose_split(long long tiles, int nkb) {
+  const long long sms = sm_count();
+  if (tiles >= sms) return 1;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int s : {1, 2, 3, 4, 8}) {
+    if (s > 1 && nkb < 4 * s) continue;
+    const double waves = (double)((tiles * s + sms - 1) / sms);
+    const double cost = waves * ((double)nkb / s + 8.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
 }
 
 template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST, int NG = TC_NG, int MINB = 1>
 cudaError_t launch_layout(const GemmArgs& g, cudaStream_t stream) {
+  const long long tiles = ((g.N + BN - 1) / BN) * ((g.M + BM - 1) / BM);
+  const int split = NACC == 1 ? choose_split(tiles, (int)(g.K / BK)) : 1;
   if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN)
-    return launch_t<AMODE, BBITS, BN, NACC, false, ST, RST, NG, MINB>(g, stream);
-  return launch_t<AMODE, BBITS, BN, NACC, true, ST, RST, NG, MINB>(g, stream);
+    return launch_t<AMODE, BBITS, BN, NACC, false, ST, RST, NG, MINB>(g, split, stream);
+  return launch_t<AMODE, BBITS, BN, NACC, true, ST, RST, NG, MINB>(g, split, stream);
 }
 
 }  // namespace
@@ -510,8 +672,10 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream) {
   if (g.act == ACT_I8 && g.bbits == 4) return launch_layout<A_I8_TMEM, 4, 256, 1, 3, 2>(g, stream);
   if (g.act == ACT_I8 && g.bbits == 2) return launch_layout<A_I8_TMEM, 2, 256, 1, 4, 2>(g, stream);
   if (g.act == ACT_F16 && g.bbits == 4) {
-    if (nkb >= 2) return launch_layout<A_F16_SMEM, 4, 256, 2, 3, 2>(g, stream);
-    return launch_layout<A_F16_SMEM, 4, 256, 1, 3, 2>(g, stream);
+    // fp32 chains of at most about half of K: two TMEM slices, or split-K
+    const long long tiles = ((g.N + 255) / 256) * ((g.M + BM - 1) / BM);
+    if (nkb < 2 || choose_split(tiles, nkb) > 1) return launch_layout<A_F16_SMEM, 4, 256, 1, 3, 2>(g, stream);
+    return launch_layout<A_F16_SMEM, 4, 256, 2, 3, 2>(g, stream);
   }
   return cudaErrorInvalidValue;
 }
