@@ -624,24 +624,14 @@ int sm_count() {
   return n[dev];
 }
 
-// Split-K factor for a grid of `tiles` output tiles of nkb k-blocks each:
-// minimise (waves of CTAs) x (k-blocks per CTA + a fixed per-CTA cost of about
-// 8 k-blocks for set-up, epilogue and the cluster reduction).  Only grids
-// smaller than one wave are split.
+// Split-K factor for a grid of `tiles` output tiles of nkb k-blocks each: the
+// largest of 2, 3, 4, 8 that keeps the grid within one wave (tiles x split <=
+// SMs) and leaves every CTA at least 4 k-blocks; 1 if none does.
 int choose_split(long long tiles, int nkb) {
   const long long sms = sm_count();
-  if (tiles >= sms) return 1;
   int best = 1;
-  double best_cost = 1e30;
-  for (int s : {1, 2, 3, 4, 8}) {
-    if (s > 1 && nkb < 4 * s) continue;
-    const double waves = (double)((tiles * s + sms - 1) / sms);
-    const double cost = waves * ((double)nkb / s + 8.0);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = s;
-    }
-  }
+  for (int s : {2, 3, 4, 8})
+    if (tiles * s <= sms && nkb >= 4 * s) best = s;
   return best;
 }
 
