@@ -29,16 +29,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Exact integer -> fp16 conversions by exponent-bias ("magic number")
 // arithmetic: a field value u in [0, 2^b) OR'ed into the low mantissa bits of
 // 1024.0 (0x6400) gives the fp16 number 1024 + u exactly; subtracting
-// 1024 + bias yields the signed value.  Two's-complement fields are first
-// made offset-binary by flipping their top bit (XOR), so u = v + bias.
+// 1024 + bias yields the signed value.  Two's-complement fields are made
+// offset-binary by flipping their top bit, so u = v + bias; for sub-byte
+// fields the flip, the mask and the OR happen in one LOP3.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
-  uint32_t r;
-  // (a & mask) | magic
-  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(a), "r"(mask), "r"(magic));
-  return r;
-}
-
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -78,30 +72,37 @@ __device__ __forceinline__ void cvt_i8x4_f16(uint32_t w, uint32_t& h01, uint32_t
   h23 = hsub2_u32(prmt(u, 0x64646464u, 0x5342u), H2_1152);
 }
 
+// (a & mask) ^ (c & mask) | (c & ~mask): with c = magic | (sign bits inside
+// the mask) this flips the top bit of every masked field (two's complement
+// -> offset binary) and ORs in the magic exponent in a single LOP3.
+__device__ __forceinline__ uint32_t lop3_flip_or(uint32_t a, uint32_t mask, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(a), "r"(mask), "r"(c));
+  return r;
+}
+
 // One interleaved 4-bit word (8 codes) -> 4 fp16x2 words in k order.
 // Field positions 0..3 hold k = 0, 2, 4, 6 and positions 4..7 hold k = 1, 3, 5, 7.
 __device__ __forceinline__ void cvt_i4x8_f16(uint32_t w, uint32_t (&h)[4]) {
-  const uint32_t x = w ^ 0x88888888u;            // u = v + 8
-  const uint32_t y = x >> 8;
-  h[0] = hsub2_u32(lop3_and_or(x, 0x000f000fu, H2_MAGIC), H2_1032);                 // k0, k1
-  h[1] = hfma2_u32(lop3_and_or(x, 0x00f000f0u, H2_MAGIC), H2_INV16, H2_NEG72);      // k2, k3
-  h[2] = hsub2_u32(lop3_and_or(y, 0x000f000fu, H2_MAGIC), H2_1032);                 // k4, k5
-  h[3] = hfma2_u32(lop3_and_or(y, 0x00f000f0u, H2_MAGIC), H2_INV16, H2_NEG72);      // k6, k7
+  const uint32_t y = w >> 8;
+  h[0] = hsub2_u32(lop3_flip_or(w, 0x000f000fu, 0x64086408u), H2_1032);                 // k0, k1
+  h[1] = hfma2_u32(lop3_flip_or(w, 0x00f000f0u, 0x64806480u), H2_INV16, H2_NEG72);      // k2, k3
+  h[2] = hsub2_u32(lop3_flip_or(y, 0x000f000fu, 0x64086408u), H2_1032);                 // k4, k5
+  h[3] = hfma2_u32(lop3_flip_or(y, 0x00f000f0u, 0x64806480u), H2_INV16, H2_NEG72);      // k6, k7
 }
 
 // One interleaved 2-bit word (16 codes) -> 8 fp16x2 words in k order.
 // Field positions 0..7 hold k = 0, 2, ..., 14 and positions 8..15 hold k = 1, 3, ..., 15.
 __device__ __forceinline__ void cvt_i2x16_f16(uint32_t w, uint32_t (&h)[8]) {
-  const uint32_t x = w ^ 0xaaaaaaaau;            // u = v + 2
-  const uint32_t y = x >> 8;
-  h[0] = hsub2_u32(lop3_and_or(x, 0x00030003u, H2_MAGIC), H2_1026);
-  h[1] = hfma2_u32(lop3_and_or(x, 0x000c000cu, H2_MAGIC), H2_INV4, H2_NEG258);
-  h[2] = hfma2_u32(lop3_and_or(x, 0x00300030u, H2_MAGIC), H2_INV16, H2_NEG66);
-  h[3] = hfma2_u32(lop3_and_or(x, 0x00c000c0u, H2_MAGIC), H2_INV64, H2_NEG18);
-  h[4] = hsub2_u32(lop3_and_or(y, 0x00030003u, H2_MAGIC), H2_1026);
-  h[5] = hfma2_u32(lop3_and_or(y, 0x000c000cu, H2_MAGIC), H2_INV4, H2_NEG258);
-  h[6] = hfma2_u32(lop3_and_or(y, 0x00300030u, H2_MAGIC), H2_INV16, H2_NEG66);
-  h[7] = hfma2_u32(lop3_and_or(y, 0x00c000c0u, H2_MAGIC), H2_INV64, H2_NEG18);
+  const uint32_t y = w >> 8;
+  h[0] = hsub2_u32(lop3_flip_or(w, 0x00030003u, 0x64026402u), H2_1026);
+  h[1] = hfma2_u32(lop3_flip_or(w, 0x000c000cu, 0x64086408u), H2_INV4, H2_NEG258);
+  h[2] = hfma2_u32(lop3_flip_or(w, 0x00300030u, 0x64206420u), H2_INV16, H2_NEG66);
+  h[3] = hfma2_u32(lop3_flip_or(w, 0x00c000c0u, 0x64806480u), H2_INV64, H2_NEG18);
+  h[4] = hsub2_u32(lop3_flip_or(y, 0x00030003u, 0x64026402u), H2_1026);
+  h[5] = hfma2_u32(lop3_flip_or(y, 0x000c000cu, 0x64086408u), H2_INV4, H2_NEG258);
+  h[6] = hfma2_u32(lop3_flip_or(y, 0x00300030u, 0x64206420u), H2_INV16, H2_NEG66);
+  h[7] = hfma2_u32(lop3_flip_or(y, 0x00c000c0u, 0x64806480u), H2_INV64, H2_NEG18);
 }
 
 // Plain-layout sub-byte word -> interleaved word (register permutation), so

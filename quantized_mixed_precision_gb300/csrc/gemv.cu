@@ -250,14 +250,13 @@ __host__ __device__ constexpr int gemv_bulk_smem(int K) {
   return 16 * (K * BBITS / 8 + WROW_PAD);
 }
 
-// 8 activation values (k0 .. k0+7) of row m as 4 fp16x2 words, or zeros.
+// 8 activation values (k0 .. k0+7) of one row (row pointer xr) as 4 fp16x2 words.
 template <int ACT>
-__device__ __forceinline__ uint4 load_x8(const void* act, int m, int K, int k0, bool valid) {
-  if (!valid) return make_uint4(0, 0, 0, 0);
+__device__ __forceinline__ uint4 load_x8(const uint8_t* xr, int k0) {
   if constexpr (ACT == ACT_F16) {
-    return __ldg(reinterpret_cast<const uint4*>(static_cast<const __half*>(act) + (size_t)m * K + k0));
+    return __ldg(reinterpret_cast<const uint4*>(xr + 2 * k0));
   } else {
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const int8_t*>(act) + (size_t)m * K + k0));
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(xr + k0));
     uint4 v;
     cvt_i8x4_f16(raw.x, v.x, v.y);
     cvt_i8x4_f16(raw.y, v.z, v.w);
@@ -265,7 +264,8 @@ __device__ __forceinline__ uint4 load_x8(const void* act, int m, int K, int k0, 
   }
 }
 
-template <int BBITS, int ACT, int NB, bool INTER>
+// FULL: K is a multiple of the step, so no thread ever reaches past K.
+template <int BBITS, int ACT, int NB, bool INTER, bool FULL>
 __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* __restrict__ act,
                                                                     const uint8_t* __restrict__ w, int M, int N, int K,
                                                                     const __half* __restrict__ row_scale,
@@ -317,6 +317,14 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   const int s_stop = w_ok ? s_end : s_begin;
   const uint8_t* wr0 = wsm + g * ws + 16 * t;
   const uint8_t* wr1 = wr0 + 8 * ws;
+  // Activation row of each MMA column: MMA columns past M read row 0 (their
+  // results are never stored), so the loads need no predicate.
+  const uint8_t* xr[NB];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    const int m = nb * 8 + g;
+    xr[nb] = static_cast<const uint8_t*>(act) + (size_t)(m < M ? m : 0) * K * (ACT == ACT_F16 ? 2 : 1);
+  }
 
   float d[2][NB][4];
 #pragma unroll
@@ -329,16 +337,22 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
 #pragma unroll 2
   for (int s = s_begin; s < s_stop; ++s) {
     const int kbase = s * C::STEP + t * C::E16;          // first k of this thread's 16 bytes
-    const bool kin = kbase < K;
+    // a ragged last step: threads past K read zero weights (and in-range activations)
+    const bool kin = FULL || kbase < K;
+    const int kx = kin ? kbase : 0;
     // activation fragments first (L1/L2 resident), overlapping the conversion
     uint4 xb[C::CPT][NB];
 #pragma unroll
     for (int j = 0; j < C::CPT; ++j)
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = load_x8<ACT>(act, nb * 8 + g, K, kbase + 8 * j, kin && nb * 8 + g < M);
+      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = load_x8<ACT>(xr[nb], kx + 8 * j);
     const uint32_t woff = (uint32_t)s * STEP_W;
-    const uint4 va = kin ? *reinterpret_cast<const uint4*>(wr0 + woff) : make_uint4(0, 0, 0, 0);
-    const uint4 vb = kin ? *reinterpret_cast<const uint4*>(wr1 + woff) : make_uint4(0, 0, 0, 0);
+    uint4 va = *reinterpret_cast<const uint4*>(wr0 + (kin ? woff : 0));
+    uint4 vb = *reinterpret_cast<const uint4*>(wr1 + (kin ? woff : 0));
+    if (!FULL && !kin) {
+      va = make_uint4(0, 0, 0, 0);
+      vb = make_uint4(0, 0, 0, 0);
+    }
     const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
     const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
@@ -386,13 +400,13 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   }
 }
 
-template <int BBITS, int ACT, int NB, bool INTER>
+template <int BBITS, int ACT, int NB, bool INTER, bool FULL>
 cudaError_t launch_bulk(const GemmArgs& g, cudaStream_t stream) {
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
   const int smem = gemv_bulk_smem<BBITS>((int)g.K);
-  auto kern = gemv_bulk_kernel<BBITS, ACT, NB, INTER>;
+  auto kern = gemv_bulk_kernel<BBITS, ACT, NB, INTER, FULL>;
   if (smem > 48 * 1024) {
     e = set_smem_once(kern, smem);
     if (e != cudaSuccess) return e;
@@ -438,9 +452,19 @@ template <int BBITS, int ACT>
 cudaError_t launch_bits_act(const GemmArgs& g, cudaStream_t stream) {
   const bool inter = g.layout == BQ_LAYOUT_INTERLEAVED;
   if (gemv_bulk_smem<BBITS>((int)g.K) <= 64 * 1024) {
-    if (g.M <= 8)
-      return inter ? launch_bulk<BBITS, ACT, 1, true>(g, stream) : launch_bulk<BBITS, ACT, 1, false>(g, stream);
-    return inter ? launch_bulk<BBITS, ACT, 2, true>(g, stream) : launch_bulk<BBITS, ACT, 2, false>(g, stream);
+    const bool full = g.K % GemvCfg<BBITS>::STEP == 0;
+    if (g.M <= 8) {
+      if (full)
+        return inter ? launch_bulk<BBITS, ACT, 1, true, true>(g, stream)
+                     : launch_bulk<BBITS, ACT, 1, false, true>(g, stream);
+      return inter ? launch_bulk<BBITS, ACT, 1, true, false>(g, stream)
+                   : launch_bulk<BBITS, ACT, 1, false, false>(g, stream);
+    }
+    if (full)
+      return inter ? launch_bulk<BBITS, ACT, 2, true, true>(g, stream)
+                   : launch_bulk<BBITS, ACT, 2, false, true>(g, stream);
+    return inter ? launch_bulk<BBITS, ACT, 2, true, false>(g, stream)
+                 : launch_bulk<BBITS, ACT, 2, false, false>(g, stream);
   }
   if (g.M <= 8) return inter ? launch_t<BBITS, ACT, 1, true>(g, stream) : launch_t<BBITS, ACT, 1, false>(g, stream);
   return inter ? launch_t<BBITS, ACT, 2, true>(g, stream) : launch_t<BBITS, ACT, 2, false>(g, stream);

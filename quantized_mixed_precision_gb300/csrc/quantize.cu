@@ -19,22 +19,22 @@ namespace {
 __device__ __forceinline__ int qmax_of(int bits) { return bits == 8 ? 127 : (bits == 4 ? 7 : 1); }
 
 // Code for one element from the stored fp16 scale s (as float) and its
-// reciprocal rcp = RN(1 / s).  In F32DIV mode the code is rne(RN(x / s)).
-// RN(x * rcp) differs from RN(x / s) by less than 2**-14 for |x / s| < 256,
-// so the two round to the same integer unless the product lies within 2**-12
-// of a half-integer; only then is the IEEE division evaluated.
+// reciprocal rcp = RN(1 / s) (0 when s == 0, which yields code 0).  In F32DIV
+// mode the code is rne(RN(x / s)).  RN(x * rcp) differs from RN(x / s) by
+// less than 2**-14 for |x / s| < 256, so both round to the same integer
+// unless the product lies within 2**-12 of a half-integer; only then is the
+// IEEE division evaluated.
 __device__ __forceinline__ int quant_one(float x, float s, float rcp, int d, int mode) {
-  if (s == 0.0f) return 0;
-  float t;
+  float r;
   if (mode == BQ_ROUND_BMINF_HALF) {
-    t = __half2float(__float2half_rn(__fdiv_rn(x, s)));
+    r = s == 0.0f ? 0.0f : rintf(__half2float(__float2half_rn(__fdiv_rn(x, s))));
   } else {
-    t = __fmul_rn(x, rcp);
-    const float frac = t - floorf(t);
-    if (fabsf(frac - 0.5f) < 2.44140625e-4f || fabsf(t) >= 256.0f) t = __fdiv_rn(x, s);
+    const float t = __fmul_rn(x, rcp);
+    r = rintf(t);                                     // nearest integer, ties to even
+    if (fabsf(t - r) > 0.5f - 2.44140625e-4f) r = rintf(__fdiv_rn(x, s));
   }
-  int r = __float2int_rn(t);  // round to nearest, ties to even
-  return r > d ? d : (r < -d ? -d : r);
+  const int q = __float2int_rn(r);
+  return q > d ? d : (q < -d ? -d : q);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -63,16 +63,15 @@ __global__ void __launch_bounds__(QT) quantize_rows_f16_kernel(const __half* __r
     const int idx = tid + QT * i;
     v[i] = idx < nvec ? __ldcs(xr + idx) : make_uint4(0, 0, 0, 0);   // streamed once
   }
-  float amax = 0.0f;
+  // |x| and max are exact in fp16: reduce packed pairs, convert once
+  __half2 m2 = __float2half2_rn(0.0f);
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __half22float2(h[j]);
-      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-    }
+    for (int j = 0; j < 4; ++j) m2 = __hmax2(m2, __habs2(h[j]));
   }
+  float amax = fmaxf(__low2float(m2), __high2float(m2));
   amax = warp_max(amax);
   if ((tid & 31) == 0) red[tid >> 5] = amax;
   __syncthreads();
@@ -94,11 +93,12 @@ __global__ void __launch_bounds__(QT) quantize_rows_f16_kernel(const __half* __r
       for (int j = 0; j < 2; ++j) {
         const float2 f0 = __half22float2(h[2 * j]);
         const float2 f1 = __half22float2(h[2 * j + 1]);
-        const uint32_t b0 = (uint32_t)(quant_one(f0.x, s, rcp, d, mode) & 0xff);
-        const uint32_t b1 = (uint32_t)(quant_one(f0.y, s, rcp, d, mode) & 0xff);
-        const uint32_t b2 = (uint32_t)(quant_one(f1.x, s, rcp, d, mode) & 0xff);
-        const uint32_t b3 = (uint32_t)(quant_one(f1.y, s, rcp, d, mode) & 0xff);
-        packed[j] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        const uint32_t b0 = (uint32_t)quant_one(f0.x, s, rcp, d, mode);
+        const uint32_t b1 = (uint32_t)quant_one(f0.y, s, rcp, d, mode);
+        const uint32_t b2 = (uint32_t)quant_one(f1.x, s, rcp, d, mode);
+        const uint32_t b3 = (uint32_t)quant_one(f1.y, s, rcp, d, mode);
+        // low bytes of the four codes -> one word
+        packed[j] = __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
       }
       __stcs(qr + idx, make_uint2(packed[0], packed[1]));
     }
