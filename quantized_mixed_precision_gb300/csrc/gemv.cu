@@ -304,18 +304,6 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // Pull this warp's activation range (its K-quarter of each row) into L1
-  // while the weights are still landing, so the per-step fragment loads hit.
-  {
-    constexpr int XB = ACT == ACT_F16 ? 2 : 1;
-    const int lines = (seg / STEP_W) * C::STEP * XB / 128;          // 128-byte lines per row
-    for (int i = lane; i < lines * M; i += 32) {
-      const int m = i / lines, l = i - m * lines;
-      const uint8_t* p = static_cast<const uint8_t*>(act) + ((size_t)m * K + (size_t)s_begin * C::STEP) * XB + 128 * l;
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-    }
-  }
-
   // Each warp waits for its own quarter; on a timeout it still waits
   // (bounded) for its copies before it may exit, and skips the math.
   bool w_ok = true;
