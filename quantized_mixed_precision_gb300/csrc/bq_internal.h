@@ -58,5 +58,9 @@ cudaError_t launch_gemv_mma(const GemmArgs& g, cudaStream_t stream);
 cudaError_t launch_gemm_dp4a(const GemmArgs& g, cudaStream_t stream);
 // Tensor-core (tcgen05) GEMM for larger M.
 cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream);
+// CTA-pair tensor-core kernel (int8 activations): the tile width it would use
+// for this problem, or 0 when the single-CTA kernel is the better fit.
+int gemm_pair_bn(const GemmArgs& g);
+cudaError_t launch_gemm_pair(const GemmArgs& g, int bn, cudaStream_t stream);
 
 }  // namespace bq

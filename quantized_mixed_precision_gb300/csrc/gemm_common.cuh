@@ -1,0 +1,69 @@
+// Pieces shared by the tensor-core GEMM kernels: host helpers, the weight-tile
+// conversion into the 128B-swizzled K-major fp16 layout that tcgen05.mma
+// reads, and a warp-uniform bounded mbarrier wait.
+#pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include "bq_device.cuh"
+
+namespace bq {
+
+// 2-D tensor map over a row-major matrix of `rows` rows of `row_elems`
+// elements (uint8, or fp16 when elem == 2); box = box_x elements x box_rows
+// rows; out-of-range elements read as zero.
+cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_elems, uint64_t rows, uint32_t box_x,
+                     uint32_t box_rows, CUtensorMapSwizzle swz);
+// Streaming multiprocessors of the current device.
+int sm_count();
+// Split-K factor the single-CTA kernel uses for `tiles` 128-row tiles of nkb
+// k-blocks (1 when the grid fills the GPU).
+int choose_split(long long tiles, int nkb);
+
+namespace {
+
+// Store one 16-byte fp16 chunk (logical chunk lc = 8 k values) of row r into a
+// 128B-swizzled K-major tile (chunk c of row r lives at position c ^ (r & 7)).
+__device__ __forceinline__ void st_chunk(uint8_t* tile, int r, int lc, uint4 v) {
+  *reinterpret_cast<uint4*>(tile + r * 128 + ((lc ^ (r & 7)) << 4)) = v;
+}
+
+// Convert one 16-byte raw weight piece (row r, piece sub) and store it.
+template <int BBITS, bool INTER>
+__device__ __forceinline__ void convert_b_piece(uint8_t* tb, int r, int sub, const uint4& v) {
+  const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (BBITS == 8) {
+    uint4 o0, o1;
+    cvt_i8x4_f16(wv[0], o0.x, o0.y);
+    cvt_i8x4_f16(wv[1], o0.z, o0.w);
+    cvt_i8x4_f16(wv[2], o1.x, o1.y);
+    cvt_i8x4_f16(wv[3], o1.z, o1.w);
+    st_chunk(tb, r, 2 * sub, o0);
+    st_chunk(tb, r, 2 * sub + 1, o1);
+  } else if constexpr (BBITS == 4) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t h[4];
+      cvt_i4x8_f16(INTER ? wv[j] : plain_to_inter_i4(wv[j]), h);
+      st_chunk(tb, r, 4 * sub + j, make_uint4(h[0], h[1], h[2], h[3]));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t h[8];
+      cvt_i2x16_f16(INTER ? wv[j] : plain_to_inter_i2(wv[j]), h);
+      st_chunk(tb, r, 8 * sub + 2 * j, make_uint4(h[0], h[1], h[2], h[3]));
+      st_chunk(tb, r, 8 * sub + 2 * j + 1, make_uint4(h[4], h[5], h[6], h[7]));
+    }
+  }
+}
+
+// Wait on an mbarrier phase with every lane of the warp; true only if all
+// lanes saw it complete (a warp-uniform decision).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, timeout_ns, status));
+}
+
+}  // namespace
+}  // namespace bq

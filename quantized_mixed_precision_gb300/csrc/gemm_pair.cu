@@ -1,0 +1,397 @@
+// Tensor-core GEMM on CTA pairs (tcgen05 cta_group::2), sm_103a.
+//
+// Same products and epilogues as the single-CTA kernel in gemm_tc.cu (int8
+// activations times int8 / 4-bit / 2-bit weights, every code converted
+// exactly to fp16, fp32 accumulation in tensor memory, fused dequantisation),
+// for the forms of the BitBLAS guide ("BitBLAS自定义操作开发指南",
+// 混合精度算子开发实战 1 and 2) and the BMINF linear ("BMINF的後訓練量化實現",
+// 實現代碼分析2).
+//
+// A 256 x BN output tile is computed by the two CTAs of a cluster with pair
+// MMAs (M = 256).  CTA r of the pair holds tile rows 128r .. 128r + 127: their
+// int8 activations, converted into its tensor memory, and their accumulators.
+// It also holds weight rows r*BN/2 .. (r+1)*BN/2 - 1 of the tile, converted
+// into its shared memory.  Each SM thus converts and stores only half of the
+// tile's weights per k-block while its tensor core does a full 128 x BN x 64
+// share of the MMA work: the weight conversion and the shared-memory traffic
+// per MMA flop are half of what one CTA per 128 x BN tile needs.
+//
+// Warp roles per CTA: NG converter groups of 12 warps, which take the
+// k-blocks in turn (group g converts kb = g mod NG), then two more warps.
+//   group warps 0-3   A: int8 activation row (thread = row = TMEM lane) ->
+//                     32 fp16 pairs -> tcgen05.st into a TMEM stage.
+//   group warps 4-11  B: raw weight codes -> fp16 128B-swizzled K-major tile.
+//   warp 12 NG        allocates tensor memory (collectively with the peer
+//                     CTA); in the even CTA its lane 0 issues the pair MMAs.
+//   warp 12 NG + 1    producer: one thread issues the TMA loads of this CTA's
+//                     raw activation and weight codes into a ring of raw stages.
+// After the mainloop the converter warps store this CTA's 128 rows of the tile.
+//
+// Handshakes: raw stages are local (TMA complete_tx -> consumers -> producer).
+// An MMA stage is ready once the 12 warps of one group of each CTA have
+// arrived on the even CTA's full barrier; the commit of the pair MMAs arrives
+// on both CTAs' empty barriers (multicast), and at the end on both
+// accumulator barriers.  Every wait is bounded in time; a wait that gives up
+// records BQ_ERR_TIMEOUT and the CTA leaves the tile.
+//
+// One CTA per SM (the shared-memory footprint guarantees it), so a CTA's
+// collective tensor-memory allocation never waits on another pair that holds
+// the same SM's tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include "bq_device.cuh"
+#include "bq_internal.h"
+#include "gemm_common.cuh"
+
+namespace bq {
+namespace {
+
+constexpr int PM = 128;                  // tile rows per CTA (256 per pair)
+constexpr int PK = 64;                   // k per block: one 128-byte fp16 swizzle row
+constexpr int P_B_THREADS = 256;         // weight converters per group
+constexpr int P_GROUP_WARPS = 12;        // one converter group: 4 activation + 8 weight warps
+constexpr uint64_t P_DRAIN_NS = 4000000000ull;
+constexpr int PAIR_NG = 2;               // converter groups per CTA (take the k-blocks in turn)
+
+template <int BBITS, int BN, int ST, int RST, int NG>
+struct PairCfg {
+  static constexpr int HB = BN / 2;                            // weight rows per CTA
+  static constexpr int CONSUMER_WARPS = NG * P_GROUP_WARPS;
+  static constexpr int MMA_WARP = CONSUMER_WARPS;
+  static constexpr int PRODUCER_WARP = MMA_WARP + 1;
+  static constexpr int THREADS = (PRODUCER_WARP + 1) * 32;
+  // a raw stage holds RKB k-blocks so that every TMA box row is 128 bytes (64 for 2-bit weights)
+  static constexpr int RKB = BBITS == 8 ? 2 : 4;
+  static constexpr int B_RAW_ROW = PK * BBITS / 8;             // raw weight bytes per row per k-block
+  static constexpr int B_BOX_X = RKB * B_RAW_ROW;
+  static constexpr int B_PIECES_ROW = B_RAW_ROW / 16;          // 16-byte pieces per row per k-block
+  static constexpr int B_PIECES = HB * B_PIECES_ROW;
+  static constexpr int NPB = (B_PIECES + P_B_THREADS - 1) / P_B_THREADS;
+  static constexpr int B_RAW = HB * B_BOX_X;
+  static constexpr int A_BOX = PM * 128;                       // int8 activations: 2 k-blocks x 128 rows
+  static constexpr int A_RAW = A_BOX * (RKB / 2);
+  static constexpr int B_TILE = HB * 128;                      // fp16 weight tile of one MMA stage
+  static constexpr int RSTAGE = A_RAW + B_RAW;
+  static constexpr int A_COLS = PK / 2;                        // TMEM columns of one activation stage
+  static constexpr int USED_COLS = BN + ST * A_COLS;
+  static constexpr int NCOLS = USED_COLS <= 256 ? 256 : 512;
+  static constexpr int OFF_RAW = ST * B_TILE;
+  static constexpr int OFF_BAR = OFF_RAW + RST * RSTAGE;
+  static constexpr size_t SMEM = (size_t)OFF_BAR + 256 + 1024;
+  static_assert(USED_COLS <= 512, "tensor memory budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(SMEM > 116 * 1024, "one CTA per SM");
+  static_assert(B_TILE % 1024 == 0 && RSTAGE % 1024 == 0 && A_RAW % 1024 == 0, "stage alignment");
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "pair MMA N and 32-column epilogue chunks");
+};
+
+template <int BBITS, int BN, bool INTER, int ST, int RST, int NG>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST, NG>::THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
+                     int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale,
+                     int epi, void* __restrict__ out, uint64_t timeout_ns, int* status) {
+  using C = PairCfg<BBITS, BN, ST, RST, NG>;
+  extern __shared__ uint8_t smem_raw[];
+  // same offset in both CTAs: the pair MMA addresses the peer's tile by this CTA's offsets
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);   // even CTA: stage filled by both
+  uint64_t* empty_bar = full_bar + ST;                                   // MMAs done with a stage
+  uint64_t* rfull_bar = empty_bar + ST;                                  // raw stage landed
+  uint64_t* rempty_bar = rfull_bar + RST;                                // raw stage read
+  uint64_t* accum_bar = rempty_bar + RST;                                // all MMAs done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int m0 = (int)(blockIdx.x >> 1) * (2 * PM) + (int)rank * PM;   // this CTA's tile rows
+  const int n0 = blockIdx.y * BN;                                      // the pair's output columns
+  const int nb0 = n0 + (int)rank * C::HB;                              // this CTA's weight rows
+  const int nkb = K / PK;
+
+  if (tid == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full_bar[s], 2 * P_GROUP_WARPS);   // one group of each CTA fills a stage
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int s = 0; s < RST; ++s) {
+      mbar_init(&rfull_bar[s], 1);
+      mbar_init(&rempty_bar[s], C::CONSUMER_WARPS * 32);   // every group releases each raw stage once
+    }
+    mbar_init(accum_bar, 1);
+    mbar_fence_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc_pair(tmem_slot, C::NCOLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == C::PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // the peer arrives on this CTA's barriers only once they are initialised
+  cluster_sync_all();
+
+  bool ok = true;
+  if (warp == C::PRODUCER_WARP) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nkb; kb += C::RKB) {
+        const int grp = kb / C::RKB, rs = grp % RST;
+        if (!mbar_wait(&rempty_bar[rs], ((grp / RST) & 1) ^ 1, timeout_ns, status)) break;
+        uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE;
+        mbar_arrive_expect_tx(&rfull_bar[rs], C::A_RAW + C::B_RAW);
+#pragma unroll
+        for (int b = 0; b < C::RKB / 2; ++b)
+          tma_load_2d(raw + b * C::A_BOX, &tmap_a, (kb + 2 * b) * PK, m0, &rfull_bar[rs]);
+        tma_load_2d(raw + C::A_RAW, &tmap_b, kb * C::B_RAW_ROW, nb0, &rfull_bar[rs]);
+        issued = grp + 1;
+      }
+      // no TMA write may land after the CTA has exited
+      for (int grp = issued > RST ? issued - RST : 0; grp < issued; ++grp)
+        mbar_wait(&rfull_bar[grp % RST], (grp / RST) & 1, P_DRAIN_NS, status);
+    }
+    __syncwarp();
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ pair MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(2 * PM, BN);
+      const uint32_t smem_base = smem_u32(smem);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % ST;
+        if (!mbar_wait_cluster(&full_bar[s], (kb / ST) & 1, timeout_ns, status)) break;
+        tc_fence_after();
+        const uint32_t a_tm = tmem + (uint32_t)(BN + s * C::A_COLS);
+        const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::B_TILE);
+#pragma unroll
+        for (int kk = 0; kk < PK / 16; ++kk)   // 16 k = 8 TMEM columns of A = +32 bytes of B
+          tc_mma_f16_ts_pair(tmem, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        tc_commit_pair(&empty_bar[s], 0x3);
+      }
+      tc_commit_pair(accum_bar, 0x3);
+      // no MMA may still be running when either CTA frees its tensor memory or exits
+      mbar_wait(accum_bar, 0, P_DRAIN_NS, status);
+    }
+    __syncwarp();
+  } else if (warp % P_GROUP_WARPS < 4) {
+    // ------------------------------------------------------------ int8 activations -> TMEM
+    // group g (warps 12g .. 12g + 11) converts the k-blocks kb = g (mod NG)
+    const int q = warp & 3;                               // TMEM lane quadrant
+    const int r = q * 32 + lane;                          // tile row == TMEM lane
+    for (int kb = warp / P_GROUP_WARPS; kb < nkb; kb += NG) {
+      const int grp = kb / C::RKB, rs = grp % RST;
+      if (!warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
+        ok = false;
+        break;
+      }
+      // this k-block is half of a 128-byte box row (128B swizzle: chunk c of row r at c ^ (r & 7))
+      const uint8_t* box = smem + C::OFF_RAW + rs * C::RSTAGE + ((kb % C::RKB) >> 1) * C::A_BOX + r * 128;
+      const int c0 = (kb & 1) * 4;
+      uint4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(box + (((c0 + j) ^ (r & 7)) << 4));
+      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
+      uint32_t h[32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        cvt_i8x4_f16(v[j].x, h[8 * j + 0], h[8 * j + 1]);
+        cvt_i8x4_f16(v[j].y, h[8 * j + 2], h[8 * j + 3]);
+        cvt_i8x4_f16(v[j].z, h[8 * j + 4], h[8 * j + 5]);
+        cvt_i8x4_f16(v[j].w, h[8 * j + 6], h[8 * j + 7]);
+      }
+      const int s = kb % ST;
+      if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) {
+        ok = false;
+        break;
+      }
+      tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN + s * C::A_COLS), h);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&full_bar[s]), 0));
+    }
+  } else {
+    // ------------------------------------------------------------ weights -> fp16 smem
+    const int c = (warp % P_GROUP_WARPS - 4) * 32 + lane;   // 0 .. 255
+    for (int kb = warp / P_GROUP_WARPS; kb < nkb; kb += NG) {
+      const int grp = kb / C::RKB, rs = grp % RST;
+      if (!warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE + C::A_RAW;
+      // piece pi is (row pi % HB, piece pi / HB): a quarter warp reads 8 rows,
+      // whose swizzled chunk positions differ (conflict-free)
+      uint4 v[C::NPB];
+#pragma unroll
+      for (int i = 0; i < C::NPB; ++i) {
+        const int pi = c + i * P_B_THREADS;
+        const int r = pi % C::HB, sub = pi / C::HB;
+        const int chunk = (kb % C::RKB) * C::B_PIECES_ROW + sub;
+        const int pos = C::B_BOX_X == 128 ? (chunk ^ (r & 7)) : (chunk ^ ((r >> 1) & 3));
+        v[i] = pi < C::B_PIECES ? *reinterpret_cast<const uint4*>(raw + r * C::B_BOX_X + (pos << 4))
+                                : make_uint4(0, 0, 0, 0);
+      }
+      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
+      const int s = kb % ST;
+      if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) {
+        ok = false;
+        break;
+      }
+      uint8_t* tb = smem + s * C::B_TILE;
+#pragma unroll
+      for (int i = 0; i < C::NPB; ++i) {
+        const int pi = c + i * P_B_THREADS;
+        if (pi < C::B_PIECES) convert_b_piece<BBITS, INTER>(tb, pi % C::HB, pi / C::HB, v[i]);
+      }
+      fence_proxy_async_smem();   // generic stores -> visible to the tensor core (async proxy)
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&full_bar[s]), 0));
+    }
+  }
+
+  // ------------------------------------------------------------ epilogue (consumer warps)
+  if (warp < C::CONSUMER_WARPS) {
+    const bool acc_ok = warp_wait(accum_bar, 0, ok ? timeout_ns : 0, status);
+    tc_fence_after();
+    if (acc_ok) {
+      // 3 * NG warps share each TMEM lane quadrant; each takes every (3 * NG)-th 32-column chunk
+      const int q = warp & 3;
+      const int part = warp >> 2;
+      const int row = m0 + 32 * q + lane;
+      const bool row_ok = row < M;
+      float rsc = 1.0f;
+      if (epi == EPI_F16_ROWCOL && row_ok) rsc = __half2float(row_scale[row]);
+#pragma unroll 1
+      for (int ch = part; ch < BN / 32; ch += 3 * NG) {
+        const int col = ch * 32;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
+        tmem_ld_wait();
+        const int ncol = n0 + col;
+        if (row_ok && ncol < N) {
+          if (epi == EPI_I32) {
+            int4* dst = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + (size_t)row * N + ncol);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_int4(__float2int_rn(__uint_as_float(r[4 * i])),
+                                 __float2int_rn(__uint_as_float(r[4 * i + 1])),
+                                 __float2int_rn(__uint_as_float(r[4 * i + 2])),
+                                 __float2int_rn(__uint_as_float(r[4 * i + 3])));
+          } else {
+            uint32_t hv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const __half2 sc2 = *reinterpret_cast<const __half2*>(col_scale + ncol + 2 * i);
+              float x0 = __fmul_rn(__uint_as_float(r[2 * i]), __low2float(sc2));
+              float x1 = __fmul_rn(__uint_as_float(r[2 * i + 1]), __high2float(sc2));
+              if (epi == EPI_F16_ROWCOL) {
+                x0 = __fmul_rn(x0, rsc);
+                x1 = __fmul_rn(x1, rsc);
+              }
+              const __half2 h2 = __halves2half2(__float2half_rn(x0), __float2half_rn(x1));
+              hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(out) + (size_t)row * N + ncol);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // the peer no longer reads this CTA's shared memory or arrives on its barriers
+  cluster_sync_all();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::NCOLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+template <int BBITS, int BN, bool INTER, int ST, int RST, int NG>
+cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
+  using C = PairCfg<BBITS, BN, ST, RST, NG>;
+  int* status = nullptr;
+  cudaError_t e = device_status_ptr(&status);
+  if (e != cudaSuccess) return e;
+  CUtensorMap ma, mb;
+  e = make_map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, 2 * PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_BOX_X, C::HB,
+               C::B_BOX_X == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+  if (e != cudaSuccess) return e;
+  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, NG>;
+  e = set_smem_once(kern, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)(2 * ((g.M + 2 * PM - 1) / (2 * PM))), (unsigned)((g.N + BN - 1) / BN));
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(ma, mb, (int)g.M, (int)g.N, (int)g.K,
+                                              reinterpret_cast<const __half*>(g.row_scale),
+                                              reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c,
+                                              (uint64_t)wait_timeout_ns(), status);
+  return cudaGetLastError();
+}
+
+template <int BBITS, int BN, int ST, int RST>
+cudaError_t launch_pair_layout(const GemmArgs& g, cudaStream_t stream) {
+  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_pair_t<BBITS, BN, false, ST, RST, PAIR_NG>(g, stream);
+  return launch_pair_t<BBITS, BN, true, ST, RST, PAIR_NG>(g, stream);
+}
+
+template <int BBITS>
+cudaError_t launch_pair_bits(const GemmArgs& g, int bn, cudaStream_t stream) {
+  constexpr int RST = BBITS == 8 ? 4 : 3;
+  switch (bn) {
+    case 256: return launch_pair_layout<BBITS, 256, 4, RST>(g, stream);
+    case 224: return launch_pair_layout<BBITS, 224, 4, RST>(g, stream);
+    case 192: return launch_pair_layout<BBITS, 192, 4, RST>(g, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int gemm_pair_bn(const GemmArgs& g) {
+  if (g.act != ACT_I8 || g.M <= 0 || g.N <= 0 || g.K < PK) return 0;
+  // int32 outputs with int8 weights accumulate exactly in one fp32 chain only up to K = 1024
+  if (g.bbits == 8 && g.epi == EPI_I32 && g.K > 1024) return 0;
+  if (g.bbits != 8 && g.bbits != 4 && g.bbits != 2) return 0;
+  // grids smaller than the GPU go to the single-CTA kernel, which splits K over clusters
+  const long long tiles1 = ((g.N + 255) / 256) * ((g.M + 127) / 128);
+  if (choose_split(tiles1, (int)(g.K / PK)) > 1) return 0;
+  // the tile width that finishes in the fewest waves of pairs, weighting a wave by its width
+  const long long pairs = sm_count() / 2;
+  const long long mp = (g.M + 2 * PM - 1) / (2 * PM);
+  int best = 0;
+  long long best_cost = 0;
+  for (int bn : {256, 224, 192}) {
+    const long long waves = (mp * ((g.N + bn - 1) / bn) + pairs - 1) / pairs;
+    const long long cost = waves * (bn + 32);
+    if (best == 0 || cost < best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_gemm_pair(const GemmArgs& g, int bn, cudaStream_t stream) {
+  if (g.bbits == 4) return launch_pair_bits<4>(g, bn, stream);
+  if (g.bbits == 2) return launch_pair_bits<2>(g, bn, stream);
+  if (g.bbits == 8) return launch_pair_bits<8>(g, bn, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace bq

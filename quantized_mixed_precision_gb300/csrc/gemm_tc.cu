@@ -42,6 +42,7 @@
 
 #include "bq_device.cuh"
 #include "bq_internal.h"
+#include "gemm_common.cuh"
 
 namespace bq {
 
@@ -78,6 +79,59 @@ cudaError_t read_device_status(int* status_out, bool reset) {
   }
   *status_out = v;
   return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// Host helpers shared by the tensor-core kernels: tensor maps, SM count,
+// split-K choice
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over a row-major matrix of `rows` rows of `row_elems` elements
+// (uint8, or fp16 when elem == 2); box = box_x elements x box_rows rows.
+// Out-of-range rows read as zero.
+cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_elems, uint64_t rows, uint32_t box_x,
+                     uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {row_elems, rows};
+  const cuuint64_t strides[1] = {row_elems * (uint64_t)elem};
+  const cuuint32_t box[2] = {box_x, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int sm_count() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!n[dev] && cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n[dev] = 148;
+  return n[dev];
+}
+
+// Split-K factor for a grid of `tiles` output tiles of nkb k-blocks each: the
+// largest of 2, 3, 4, 8 that keeps the grid within one wave (tiles x split <=
+// SMs) and leaves every CTA at least 4 k-blocks; 1 if none does.
+int choose_split(long long tiles, int nkb) {
+  const long long sms = sm_count();
+  int best = 1;
+  for (int s : {2, 3, 4, 8})
+    if (tiles * s <= sms && nkb >= 4 * s) best = s;
+  return best;
 }
 
 namespace {
@@ -130,48 +184,6 @@ struct Cfg {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert((BN / (2 * NG)) % 32 == 0, "epilogue column parts are whole 32-column chunks");
 };
-
-// Store one 16-byte fp16 chunk (logical chunk lc = 8 k values) of row r into a
-// 128B-swizzled K-major tile (chunk c of row r lives at position c ^ (r & 7)).
-__device__ __forceinline__ void st_chunk(uint8_t* tile, int r, int lc, uint4 v) {
-  *reinterpret_cast<uint4*>(tile + r * 128 + ((lc ^ (r & 7)) << 4)) = v;
-}
-
-// Convert one 16-byte raw weight piece (row r, piece sub) and store it.
-template <int BBITS, bool INTER>
-__device__ __forceinline__ void convert_b_piece(uint8_t* tb, int r, int sub, const uint4& v) {
-  const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-  if constexpr (BBITS == 8) {
-    uint4 o0, o1;
-    cvt_i8x4_f16(wv[0], o0.x, o0.y);
-    cvt_i8x4_f16(wv[1], o0.z, o0.w);
-    cvt_i8x4_f16(wv[2], o1.x, o1.y);
-    cvt_i8x4_f16(wv[3], o1.z, o1.w);
-    st_chunk(tb, r, 2 * sub, o0);
-    st_chunk(tb, r, 2 * sub + 1, o1);
-  } else if constexpr (BBITS == 4) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t h[4];
-      cvt_i4x8_f16(INTER ? wv[j] : plain_to_inter_i4(wv[j]), h);
-      st_chunk(tb, r, 4 * sub + j, make_uint4(h[0], h[1], h[2], h[3]));
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t h[8];
-      cvt_i2x16_f16(INTER ? wv[j] : plain_to_inter_i2(wv[j]), h);
-      st_chunk(tb, r, 8 * sub + 2 * j, make_uint4(h[0], h[1], h[2], h[3]));
-      st_chunk(tb, r, 8 * sub + 2 * j + 1, make_uint4(h[4], h[5], h[6], h[7]));
-    }
-  }
-}
-
-// Wait on an mbarrier phase with every lane of the warp; true only if all
-// lanes saw it complete (a warp-uniform decision).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int* status) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, timeout_ns, status));
-}
 
 template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST, int NG, int MINB>
 __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>::THREADS, MINB)
@@ -540,38 +552,8 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
 }
 
 // ---------------------------------------------------------------------------
-// Host side: tensor maps and launch
+// Host side: launch
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2-D map over a row-major matrix of `rows` rows of `row_elems` elements
-// (uint8, or fp16 when elem == 2); box = box_x elements x box_rows rows.
-// Out-of-range rows read as zero.
-cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_elems, uint64_t rows, uint32_t box_x,
-                     uint32_t box_rows, CUtensorMapSwizzle swz) {
-  auto fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {row_elems, rows};
-  const cuuint64_t strides[1] = {row_elems * (uint64_t)elem};
-  const cuuint32_t box[2] = {box_x, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST, int NG, int MINB>
 cudaError_t launch_t(const GemmArgs& g, int split, cudaStream_t stream) {
   using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>;
@@ -616,25 +598,6 @@ cudaError_t launch_t(const GemmArgs& g, int split, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-int sm_count() {
-  static int n[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!n[dev] && cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n[dev] = 148;
-  return n[dev];
-}
-
-// Split-K factor for a grid of `tiles` output tiles of nkb k-blocks each: the
-// largest of 2, 3, 4, 8 that keeps the grid within one wave (tiles x split <=
-// SMs) and leaves every CTA at least 4 k-blocks; 1 if none does.
-int choose_split(long long tiles, int nkb) {
-  const long long sms = sm_count();
-  int best = 1;
-  for (int s : {2, 3, 4, 8})
-    if (tiles * s <= sms && nkb >= 4 * s) best = s;
-  return best;
-}
-
 template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST, int NG = TC_NG, int MINB = 1>
 cudaError_t launch_layout(const GemmArgs& g, cudaStream_t stream) {
   const long long tiles = ((g.N + BN - 1) / BN) * ((g.M + BM - 1) / BM);
@@ -648,6 +611,7 @@ cudaError_t launch_layout(const GemmArgs& g, cudaStream_t stream) {
 
 cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream) {
   const int nkb = (int)(g.K / BK);
+  if (const int bn = gemm_pair_bn(g)) return launch_gemm_pair(g, bn, stream);
   if (g.act == ACT_I8 && g.bbits == 8) {
     if (g.epi == EPI_I32) {
       // int32 output: slices of at most 1024 k keep every partial sum < 2**24 exactly
