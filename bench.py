@@ -319,7 +319,7 @@ def run_gpu(args, rank, world, local_rank):
 
     paths = {} if args.no_paths else measure_paths(torch, bq, W, roofline, dev, flush, stream, hbm_peak, tc_peak)
     achieved = OPS2 / (ms_step * 1e-3) / 1e12
-    traffic = ncu_traffic("gemm_tc_kernel")
+    traffic = ncu_traffic("gemm_pair_kernel")
     line = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -328,12 +328,12 @@ def run_gpu(args, rank, world, local_rank):
                    "l2": "inputs larger than L2: steps cycle through 3 input sets (168 MiB); K steps replayed as one "
                          "CUDA graph between two events",
                    "single_launch_ms_l2_flushed": statistics.median(single),
-                   "mma": "tcgen05.mma kind::f16 (int8/int4 converted exactly to fp16), fp32 accumulation",
+                   "mma": "tcgen05.mma cta_group::2 kind::f16 on CTA pairs (int8/int4 converted exactly to fp16), fp32 accumulation",
                    "per_gpu": "independent replica of the workload on every rank"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak, "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops (burst; fp16 dense rate equals bf16)",
-                     "kernel": "gemm_tc_kernel"},
+                     "kernel": "gemm_pair_kernel"},
         "e2e": e2e, "gpu_launches": gemm_launches_per_step * args.steps, "clocks": clocks,
         "wall_s_timed_region": t_wall, "gemv": gemv, "paths": paths,
     }

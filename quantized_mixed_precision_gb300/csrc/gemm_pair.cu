@@ -161,21 +161,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ pair MMA issuer (even CTA)
-    if (rank == 0 && lane == 0) {
+    // The whole warp runs the loop, so the operand addresses are warp-uniform;
+    // one elected lane issues the MMAs and their commits.
+    if (rank == 0) {
+      const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+      const uint32_t smem_base = __shfl_sync(0xffffffffu, smem_u32(smem), 0);
       const uint32_t idesc = idesc_f16_f32(2 * PM, BN);
-      const uint32_t smem_base = smem_u32(smem);
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % ST;
-        if (!mbar_wait_cluster(&full_bar[s], (kb / ST) & 1, timeout_ns, status)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(&full_bar[s], (kb / ST) & 1, timeout_ns, status))) break;
         tc_fence_after();
-        const uint32_t a_tm = tmem + (uint32_t)(BN + s * C::A_COLS);
+        const uint32_t a_tm = tm + (uint32_t)(BN + s * C::A_COLS);
         const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::B_TILE);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < PK / 16; ++kk)   // 16 k = 8 TMEM columns of A = +32 bytes of B
-          tc_mma_f16_ts_pair(tmem, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-        tc_commit_pair(&empty_bar[s], 0x3);
+          for (int kk = 0; kk < PK / 16; ++kk)   // 16 k = 8 TMEM columns of A = +32 bytes of B
+            tc_mma_f16_ts_pair(tm, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit_pair(&empty_bar[s], 0x3);
+        }
+        __syncwarp();
       }
-      tc_commit_pair(accum_bar, 0x3);
+      if (elect_one()) tc_commit_pair(accum_bar, 0x3);
+      __syncwarp();
       // no MMA may still be running when either CTA frees its tensor memory or exits
       mbar_wait(accum_bar, 0, P_DRAIN_NS, status);
     }

@@ -283,34 +283,39 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(BM, BN);
-      const uint32_t smem_base = smem_u32(smem);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % ST;
-        if (!mbar_wait(&full_bar[s], (kb / ST) & 1, timeout_ns, status)) break;
-        tc_fence_after();
-        const int slice = (int)(((long long)kb * NACC) / nkb);
-        const bool first = kb == 0 || slice != (int)(((long long)(kb - 1) * NACC) / nkb);
-        const uint32_t d = tmem + (uint32_t)(slice * BN);
-        const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::STAGE + C::A_TILE);
+    // The whole warp runs the loop, so the operand addresses are warp-uniform;
+    // one elected lane issues the MMAs and their commits.
+    const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+    const uint32_t smem_base = __shfl_sync(0xffffffffu, smem_u32(smem), 0);
+    const uint32_t idesc = idesc_f16_f32(BM, BN);
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % ST;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], (kb / ST) & 1, timeout_ns, status))) break;
+      tc_fence_after();
+      const int slice = (int)(((long long)kb * NACC) / nkb);
+      const bool first = kb == 0 || slice != (int)(((long long)(kb - 1) * NACC) / nkb);
+      const uint32_t d = tm + (uint32_t)(slice * BN);
+      const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::STAGE + C::A_TILE);
+      if (elect_one()) {
         if constexpr (AMODE == A_F16_SMEM) {
           const uint64_t adesc = smem_desc_sw128(smem_base + s * C::STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K = +2 in the address field
             tc_mma_f16(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
         } else {
-          const uint32_t a_tm = tmem + (uint32_t)(C::ACC_COLS + s * C::A_COLS);
+          const uint32_t a_tm = tm + (uint32_t)(C::ACC_COLS + s * C::A_COLS);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)   // 16 k = 8 TMEM columns of A
             tc_mma_f16_ts(d, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
         }
         tc_commit(&empty_bar[s]);
       }
-      tc_commit(accum_bar);
-      // no MMA may still be running when the tensor memory is freed
-      mbar_wait(accum_bar, 0, DRAIN_TIMEOUT_NS, status);
+      __syncwarp();
     }
+    if (elect_one()) tc_commit(accum_bar);
+    __syncwarp();
+    // no MMA may still be running when the tensor memory is freed
+    mbar_wait(accum_bar, 0, DRAIN_TIMEOUT_NS, status);
     __syncwarp();
   } else if (warp < C::A_WARPS) {
     // ------------------------------------------------------------ int8 A -> TMEM
