@@ -16,20 +16,25 @@
 // share of the MMA work: the weight conversion and the shared-memory traffic
 // per MMA flop are half of what one CTA per 128 x BN tile needs.
 //
-// Warp roles per CTA: NG converter groups of 12 warps, which take the
-// k-blocks in turn (group g converts kb = g mod NG), then two more warps.
-//   group warps 0-3   A: int8 activation row (thread = row = TMEM lane) ->
-//                     32 fp16 pairs -> tcgen05.st into a TMEM stage.
-//   group warps 4-11  B: raw weight codes -> fp16 128B-swizzled K-major tile.
-//   warp 12 NG        allocates tensor memory (collectively with the peer
-//                     CTA); in the even CTA its lane 0 issues the pair MMAs.
-//   warp 12 NG + 1    producer: one thread issues the TMA loads of this CTA's
-//                     raw activation and weight codes into a ring of raw stages.
+// Warp roles per CTA.  The converters come in groups that take the k-blocks
+// in turn (group g of n converts kb = g mod n), so the fixed cost of each
+// k-block's waits and arrivals overlaps across groups:
+//   P_NA groups of 4 warps    A: int8 activation row (thread = row = TMEM
+//                             lane) -> 32 fp16 pairs -> tcgen05.st into a
+//                             TMEM stage.
+//   P_NB groups of P_BW warps B: raw weight codes -> fp16 128B-swizzled
+//                             K-major tile in shared memory.
+//   next warp                 allocates tensor memory (collectively with the
+//                             peer CTA); in the even CTA one elected lane
+//                             issues the pair MMAs.
+//   last warp                 producer: one thread issues the TMA loads of
+//                             this CTA's raw activation and weight codes into
+//                             a ring of raw stages.
 // After the mainloop the converter warps store this CTA's 128 rows of the tile.
 //
 // Handshakes: raw stages are local (TMA complete_tx -> consumers -> producer).
-// An MMA stage is ready once the 12 warps of one group of each CTA have
-// arrived on the even CTA's full barrier; the commit of the pair MMAs arrives
+// An MMA stage is ready once one A group and one B group of each CTA have
+// arrived on the even CTA's full barrier (one arrival per warp); the commit of the pair MMAs arrives
 // on both CTAs' empty barriers (multicast), and at the end on both
 // accumulator barriers.  Every wait is bounded in time; a wait that gives up
 // records BQ_ERR_TIMEOUT and the CTA leaves the tile.
@@ -50,15 +55,17 @@ namespace {
 
 constexpr int PM = 128;                  // tile rows per CTA (256 per pair)
 constexpr int PK = 64;                   // k per block: one 128-byte fp16 swizzle row
-constexpr int P_B_THREADS = 256;         // weight converters per group
-constexpr int P_GROUP_WARPS = 12;        // one converter group: 4 activation + 8 weight warps
+constexpr int P_NA = 2;                  // activation converter groups (4 warps each)
+constexpr int P_NB = 4;                  // weight converter groups
+constexpr int P_BW = 4;                  // warps per weight converter group
+constexpr int P_A_WARPS = 4 * P_NA;
+constexpr int P_B_THREADS = P_BW * 32;   // weight converters per group
 constexpr uint64_t P_DRAIN_NS = 4000000000ull;
-constexpr int PAIR_NG = 2;               // converter groups per CTA (take the k-blocks in turn)
 
-template <int BBITS, int BN, int ST, int RST, int NG>
+template <int BBITS, int BN, int ST, int RST>
 struct PairCfg {
   static constexpr int HB = BN / 2;                            // weight rows per CTA
-  static constexpr int CONSUMER_WARPS = NG * P_GROUP_WARPS;
+  static constexpr int CONSUMER_WARPS = P_A_WARPS + P_NB * P_BW;
   static constexpr int MMA_WARP = CONSUMER_WARPS;
   static constexpr int PRODUCER_WARP = MMA_WARP + 1;
   static constexpr int THREADS = (PRODUCER_WARP + 1) * 32;
@@ -78,6 +85,10 @@ struct PairCfg {
   static constexpr int USED_COLS = BN + ST * A_COLS;
   static constexpr int NCOLS = USED_COLS <= 256 ? 256 : 512;
   static constexpr int OFF_RAW = ST * B_TILE;
+  // threads that read one (full) raw stage: a stage of RKB k-blocks is read by
+  // min(groups, RKB) groups of each kind
+  static constexpr int RAW_READERS =
+      (P_NA < RKB ? P_NA : RKB) * 4 * 32 + (P_NB < RKB ? P_NB : RKB) * P_B_THREADS;
   static constexpr int OFF_BAR = OFF_RAW + RST * RSTAGE;
   static constexpr size_t SMEM = (size_t)OFF_BAR + 256 + 1024;
   static_assert(USED_COLS <= 512, "tensor memory budget");
@@ -85,14 +96,19 @@ struct PairCfg {
   static_assert(SMEM > 116 * 1024, "one CTA per SM");
   static_assert(B_TILE % 1024 == 0 && RSTAGE % 1024 == 0 && A_RAW % 1024 == 0, "stage alignment");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "pair MMA N and 32-column epilogue chunks");
+  static_assert(CONSUMER_WARPS % 4 == 0 && THREADS <= 1024, "warp roles");
+  // A group that has finished k-block kb - n (n groups) knows that the MMAs of
+  // kb - n - ST are done; its wait for the stage of kb must not pass on the
+  // parity of a phase two behind, which needs n <= ST.
+  static_assert(P_NA <= ST && P_NB <= ST, "converter groups per stage ring");
 };
 
-template <int BBITS, int BN, bool INTER, int ST, int RST, int NG>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST, NG>::THREADS, 1)
+template <int BBITS, int BN, bool INTER, int ST, int RST>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
                      int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale,
                      int epi, void* __restrict__ out, uint64_t timeout_ns, int* status) {
-  using C = PairCfg<BBITS, BN, ST, RST, NG>;
+  using C = PairCfg<BBITS, BN, ST, RST>;
   extern __shared__ uint8_t smem_raw[];
   // same offset in both CTAs: the pair MMA addresses the peer's tile by this CTA's offsets
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -113,12 +129,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
-      mbar_init(&full_bar[s], 2 * P_GROUP_WARPS);   // one group of each CTA fills a stage
+      mbar_init(&full_bar[s], 2 * (4 + P_BW));   // one A and one B group of each CTA fill a stage
       mbar_init(&empty_bar[s], 1);
     }
     for (int s = 0; s < RST; ++s) {
       mbar_init(&rfull_bar[s], 1);
-      mbar_init(&rempty_bar[s], C::CONSUMER_WARPS * 32);   // every group releases each raw stage once
+      mbar_init(&rempty_bar[s], C::RAW_READERS);   // every group that reads a raw stage releases it once
     }
     mbar_init(accum_bar, 1);
     mbar_fence_init();
@@ -187,14 +203,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       mbar_wait(accum_bar, 0, P_DRAIN_NS, status);
     }
     __syncwarp();
-  } else if (warp % P_GROUP_WARPS < 4) {
+  } else if (warp < P_A_WARPS) {
     // ------------------------------------------------------------ int8 activations -> TMEM
-    // group g (warps 12g .. 12g + 11) converts the k-blocks kb = g (mod NG)
+    // A group g (warps 4g .. 4g + 3) converts the k-blocks kb = g (mod P_NA)
     const int q = warp & 3;                               // TMEM lane quadrant
     const int r = q * 32 + lane;                          // tile row == TMEM lane
-    for (int kb = warp / P_GROUP_WARPS; kb < nkb; kb += NG) {
+    for (int kb = warp >> 2; kb < nkb; kb += P_NA) {
       const int grp = kb / C::RKB, rs = grp % RST;
-      if (!warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
+      // the group's first k-block of a raw stage waits for it to land
+      if (kb % C::RKB < P_NA && !warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
         ok = false;
         break;
       }
@@ -204,7 +221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       uint4 v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(box + (((c0 + j) ^ (r & 7)) << 4));
-      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
+      if ((kb % C::RKB) + P_NA >= C::RKB || kb + P_NA >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
       uint32_t h[32];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -226,10 +243,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
     }
   } else {
     // ------------------------------------------------------------ weights -> fp16 smem
-    const int c = (warp % P_GROUP_WARPS - 4) * 32 + lane;   // 0 .. 255
-    for (int kb = warp / P_GROUP_WARPS; kb < nkb; kb += NG) {
+    // B group g (warps P_A_WARPS + g * P_BW ..) converts the k-blocks kb = g (mod P_NB)
+    const int bw = warp - P_A_WARPS;
+    const int c = (bw % P_BW) * 32 + lane;                // converter thread within its group
+    for (int kb = bw / P_BW; kb < nkb; kb += P_NB) {
       const int grp = kb / C::RKB, rs = grp % RST;
-      if (!warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
+      if (kb % C::RKB < P_NB && !warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
         ok = false;
         break;
       }
@@ -246,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         v[i] = pi < C::B_PIECES ? *reinterpret_cast<const uint4*>(raw + r * C::B_BOX_X + (pos << 4))
                                 : make_uint4(0, 0, 0, 0);
       }
-      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
+      if ((kb % C::RKB) + P_NB >= C::RKB || kb + P_NB >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
       const int s = kb % ST;
       if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) {
         ok = false;
@@ -269,7 +288,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
     const bool acc_ok = warp_wait(accum_bar, 0, ok ? timeout_ns : 0, status);
     tc_fence_after();
     if (acc_ok) {
-      // 3 * NG warps share each TMEM lane quadrant; each takes every (3 * NG)-th 32-column chunk
+      // CONSUMER_WARPS / 4 warps share each TMEM lane quadrant; each takes every such 32-column chunk
       const int q = warp & 3;
       const int part = warp >> 2;
       const int row = m0 + 32 * q + lane;
@@ -277,7 +296,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       float rsc = 1.0f;
       if (epi == EPI_F16_ROWCOL && row_ok) rsc = __half2float(row_scale[row]);
 #pragma unroll 1
-      for (int ch = part; ch < BN / 32; ch += 3 * NG) {
+      for (int ch = part; ch < BN / 32; ch += C::CONSUMER_WARPS / 4) {
         const int col = ch * 32;
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
@@ -328,9 +347,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-template <int BBITS, int BN, bool INTER, int ST, int RST, int NG>
+template <int BBITS, int BN, bool INTER, int ST, int RST>
 cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
-  using C = PairCfg<BBITS, BN, ST, RST, NG>;
+  using C = PairCfg<BBITS, BN, ST, RST>;
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
@@ -340,7 +359,7 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_BOX_X, C::HB,
                C::B_BOX_X == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, NG>;
+  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST>;
   e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(2 * ((g.M + 2 * PM - 1) / (2 * PM))), (unsigned)((g.N + BN - 1) / BN));
@@ -353,8 +372,8 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
 
 template <int BBITS, int BN, int ST, int RST>
 cudaError_t launch_pair_layout(const GemmArgs& g, cudaStream_t stream) {
-  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_pair_t<BBITS, BN, false, ST, RST, PAIR_NG>(g, stream);
-  return launch_pair_t<BBITS, BN, true, ST, RST, PAIR_NG>(g, stream);
+  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_pair_t<BBITS, BN, false, ST, RST>(g, stream);
+  return launch_pair_t<BBITS, BN, true, ST, RST>(g, stream);
 }
 
 template <int BBITS>
