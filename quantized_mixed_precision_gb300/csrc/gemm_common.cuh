@@ -11,8 +11,9 @@
 namespace bq {
 
 // 2-D tensor map over a row-major matrix of `rows` rows of `row_elems`
-// elements (uint8, or fp16 when elem == 2); box = box_x elements x box_rows
-// rows; out-of-range elements read as zero.
+// elements (uint8, fp16 when elem == 2, int32 when elem == 4); box = box_x
+// elements x box_rows rows; out-of-range elements read as zero and are not
+// written by stores.
 cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_elems, uint64_t rows, uint32_t box_x,
                      uint32_t box_rows, CUtensorMapSwizzle swz);
 // Streaming multiprocessors of the current device.

@@ -85,6 +85,7 @@ struct PairCfg {
   static constexpr int USED_COLS = BN + ST * A_COLS;
   static constexpr int NCOLS = USED_COLS <= 256 ? 256 : 512;
   static constexpr int OFF_RAW = ST * B_TILE;
+  static constexpr int STG_BYTES = 32 * 32 * 4;                // epilogue staging box per warp (int32)
   // threads that read one (full) raw stage: a stage of RKB k-blocks is read by
   // min(groups, RKB) groups of each kind
   static constexpr int RAW_READERS =
@@ -101,13 +102,15 @@ struct PairCfg {
   // kb - n - ST are done; its wait for the stage of kb must not pass on the
   // parity of a phase two behind, which needs n <= ST.
   static_assert(P_NA <= ST && P_NB <= ST, "converter groups per stage ring");
+  static_assert(CONSUMER_WARPS * STG_BYTES <= OFF_BAR, "epilogue staging fits in the pipeline buffers");
 };
 
 template <int BBITS, int BN, bool INTER, int ST, int RST>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST>::THREADS, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
-                     int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale,
-                     int epi, void* __restrict__ out, uint64_t timeout_ns, int* status) {
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                     const __grid_constant__ CUtensorMap tmap_c, int M, int N, int K,
+                     const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
+                     uint64_t timeout_ns, int* status) {
   using C = PairCfg<BBITS, BN, ST, RST>;
   extern __shared__ uint8_t smem_raw[];
   // same offset in both CTAs: the pair MMA addresses the peer's tile by this CTA's offsets
@@ -288,49 +291,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
     const bool acc_ok = warp_wait(accum_bar, 0, ok ? timeout_ns : 0, status);
     tc_fence_after();
     if (acc_ok) {
-      // CONSUMER_WARPS / 4 warps share each TMEM lane quadrant; each takes every such 32-column chunk
+      // CONSUMER_WARPS / 4 warps share each TMEM lane quadrant; each takes
+      // every such 32-column chunk.  The pipeline buffers are idle now: each
+      // warp stages its 32 x 32 output boxes in its own 4 KB of them (rows
+      // swizzled like the tensor map) and stores them with TMA.
       const int q = warp & 3;
       const int part = warp >> 2;
-      const int row = m0 + 32 * q + lane;
-      const bool row_ok = row < M;
+      const int row0 = m0 + 32 * q;
+      const int row = row0 + lane;
       float rsc = 1.0f;
-      if (epi == EPI_F16_ROWCOL && row_ok) rsc = __half2float(row_scale[row]);
+      if (epi == EPI_F16_ROWCOL && row < M) rsc = __half2float(row_scale[row]);
+      uint8_t* stg = smem + warp * C::STG_BYTES;
 #pragma unroll 1
-      for (int ch = part; ch < BN / 32; ch += C::CONSUMER_WARPS / 4) {
+      for (int ch = part; ch < BN / 32 && row0 < M; ch += C::CONSUMER_WARPS / 4) {
         const int col = ch * 32;
+        const int ncol = n0 + col;
+        if (ncol >= N) break;
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
         tmem_ld_wait();
-        const int ncol = n0 + col;
-        if (row_ok && ncol < N) {
-          if (epi == EPI_I32) {
-            int4* dst = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + (size_t)row * N + ncol);
+        if (lane == 0) bulk_wait_read_all();   // the previous box has left the staging buffer
+        __syncwarp();
+        if (epi == EPI_I32) {
+          // row `lane`: 32 int32 = 8 chunks of 16 bytes; 128B swizzle (chunk j at j ^ (lane & 7))
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_int4(__float2int_rn(__uint_as_float(r[4 * i])),
-                                 __float2int_rn(__uint_as_float(r[4 * i + 1])),
-                                 __float2int_rn(__uint_as_float(r[4 * i + 2])),
-                                 __float2int_rn(__uint_as_float(r[4 * i + 3])));
-          } else {
-            uint32_t hv[16];
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<int4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_int4(__float2int_rn(__uint_as_float(r[4 * j])), __float2int_rn(__uint_as_float(r[4 * j + 1])),
+                          __float2int_rn(__uint_as_float(r[4 * j + 2])),
+                          __float2int_rn(__uint_as_float(r[4 * j + 3])));
+        } else {
+          uint32_t hv[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const __half2 sc2 = *reinterpret_cast<const __half2*>(col_scale + ncol + 2 * i);
-              float x0 = __fmul_rn(__uint_as_float(r[2 * i]), __low2float(sc2));
-              float x1 = __fmul_rn(__uint_as_float(r[2 * i + 1]), __high2float(sc2));
-              if (epi == EPI_F16_ROWCOL) {
-                x0 = __fmul_rn(x0, rsc);
-                x1 = __fmul_rn(x1, rsc);
-              }
-              const __half2 h2 = __halves2half2(__float2half_rn(x0), __float2half_rn(x1));
-              hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
+          for (int i = 0; i < 16; ++i) {
+            const __half2 sc2 = *reinterpret_cast<const __half2*>(col_scale + ncol + 2 * i);
+            float x0 = __fmul_rn(__uint_as_float(r[2 * i]), __low2float(sc2));
+            float x1 = __fmul_rn(__uint_as_float(r[2 * i + 1]), __high2float(sc2));
+            if (epi == EPI_F16_ROWCOL) {
+              x0 = __fmul_rn(x0, rsc);
+              x1 = __fmul_rn(x1, rsc);
             }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(out) + (size_t)row * N + ncol);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+            const __half2 h2 = __halves2half2(__float2half_rn(x0), __float2half_rn(x1));
+            hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
           }
+          // row `lane`: 32 fp16 = 4 chunks of 16 bytes; 64B swizzle (chunk j at j ^ ((lane >> 1) & 3))
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]);
+        }
+        fence_proxy_async_smem();   // generic stores -> visible to the TMA engine
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_c, stg, ncol, row0);   // rows past M are not written
+          bulk_commit_group();
         }
       }
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
 
@@ -353,19 +371,25 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc;
   e = make_map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, 2 * PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_BOX_X, C::HB,
                C::B_BOX_X == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
+  // output boxes of 32 x 32: int32 rows of 128 bytes, fp16 rows of 64 bytes
+  if (g.epi == EPI_I32)
+    e = make_map(&mc, g.c, 4, (uint64_t)g.N, (uint64_t)g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    e = make_map(&mc, g.c, 2, (uint64_t)g.N, (uint64_t)g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (e != cudaSuccess) return e;
   auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST>;
   e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(2 * ((g.M + 2 * PM - 1) / (2 * PM))), (unsigned)((g.N + BN - 1) / BN));
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(ma, mb, (int)g.M, (int)g.N, (int)g.K,
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(ma, mb, mc, (int)g.M, (int)g.N, (int)g.K,
                                               reinterpret_cast<const __half*>(g.row_scale),
-                                              reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c,
+                                              reinterpret_cast<const __half*>(g.col_scale), g.epi,
                                               (uint64_t)wait_timeout_ns(), status);
   return cudaGetLastError();
 }

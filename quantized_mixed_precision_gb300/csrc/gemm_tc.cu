@@ -99,8 +99,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D map over a row-major matrix of `rows` rows of `row_elems` elements
-// (uint8, or fp16 when elem == 2); box = box_x elements x box_rows rows.
-// Out-of-range rows read as zero.
+// (uint8, fp16 when elem == 2, int32 when elem == 4); box = box_x elements x
+// box_rows rows.  Out-of-range elements read as zero and are not written.
 cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_elems, uint64_t rows, uint32_t box_x,
                      uint32_t box_rows, CUtensorMapSwizzle swz) {
   auto fn = encode_fn();
@@ -109,7 +109,10 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_
   const cuuint64_t strides[1] = {row_elems * (uint64_t)elem};
   const cuuint32_t box[2] = {box_x, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+  const CUtensorMapDataType dt = elem == 4   ? CU_TENSOR_MAP_DATA_TYPE_INT32
+                                 : elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = fn(map, dt, 2,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
