@@ -406,6 +406,19 @@ __device__ __forceinline__ void tc_mma_f16_ts_pair(uint32_t d_tmem, uint32_t a_t
       : "memory");
 }
 
+// Pair MMA with both operands in shared memory: A's 256 rows split like D
+// (rows 0-127 in the even CTA's shared memory, 128-255 in the odd CTA's), B as
+// for the tensor-memory form; all at the same offsets in both CTAs.
+__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the mbarrier at the same shared-memory offset in every CTA
 // of cta_mask when all pair MMAs issued so far by this thread complete.
 __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {

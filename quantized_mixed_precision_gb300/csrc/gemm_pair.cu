@@ -62,10 +62,16 @@ constexpr int P_A_WARPS = 4 * P_NA;
 constexpr int P_B_THREADS = P_BW * 32;   // weight converters per group
 constexpr uint64_t P_DRAIN_NS = 4000000000ull;
 
-template <int BBITS, int BN, int ST, int RST>
+// AF16: fp16 activations, loaded by TMA straight into the MMA's 128B-swizzled
+// K-major layout (no activation converters, A read from shared memory), and
+// two accumulator slices of half of K each (shorter fp32 chains).  Otherwise
+// int8 activations, converted into tensor memory, one accumulator.
+template <int BBITS, int BN, int ST, int RST, bool AF16>
 struct PairCfg {
   static constexpr int HB = BN / 2;                            // weight rows per CTA
-  static constexpr int CONSUMER_WARPS = P_A_WARPS + P_NB * P_BW;
+  static constexpr int A_WARPS = AF16 ? 0 : P_A_WARPS;
+  static constexpr int NA = AF16 ? 0 : P_NA;                   // activation converter groups
+  static constexpr int CONSUMER_WARPS = A_WARPS + P_NB * P_BW;
   static constexpr int MMA_WARP = CONSUMER_WARPS;
   static constexpr int PRODUCER_WARP = MMA_WARP + 1;
   static constexpr int THREADS = (PRODUCER_WARP + 1) * 32;
@@ -78,26 +84,33 @@ struct PairCfg {
   static constexpr int NPB = (B_PIECES + P_B_THREADS - 1) / P_B_THREADS;
   static constexpr int B_RAW = HB * B_BOX_X;
   static constexpr int A_BOX = PM * 128;                       // int8 activations: 2 k-blocks x 128 rows
-  static constexpr int A_RAW = A_BOX * (RKB / 2);
+  static constexpr int A_RAW = AF16 ? 0 : A_BOX * (RKB / 2);
+  static constexpr int A_TILE = AF16 ? PM * 128 : 0;           // fp16 activation tile of one MMA stage
   static constexpr int B_TILE = HB * 128;                      // fp16 weight tile of one MMA stage
+  static constexpr int STAGE = A_TILE + B_TILE;
   static constexpr int RSTAGE = A_RAW + B_RAW;
+  static constexpr int NACC = AF16 ? 2 : 1;                    // accumulator slices
   static constexpr int A_COLS = PK / 2;                        // TMEM columns of one activation stage
-  static constexpr int USED_COLS = BN + ST * A_COLS;
+  static constexpr int ACC_COLS = NACC * BN;
+  static constexpr int USED_COLS = ACC_COLS + (AF16 ? 0 : ST * A_COLS);
   static constexpr int NCOLS = USED_COLS <= 256 ? 256 : 512;
-  static constexpr int OFF_RAW = ST * B_TILE;
+  static constexpr int OFF_RAW = ST * STAGE;
   static constexpr int STG_BYTES = 32 * 32 * 4;                // epilogue staging box per warp (int32)
   // threads that read one (full) raw stage: a stage of RKB k-blocks is read by
   // min(groups, RKB) groups of each kind
   static constexpr int RAW_READERS =
-      (P_NA < RKB ? P_NA : RKB) * 4 * 32 + (P_NB < RKB ? P_NB : RKB) * P_B_THREADS;
+      (NA < RKB ? NA : RKB) * 4 * 32 + (P_NB < RKB ? P_NB : RKB) * P_B_THREADS;
+  // arrivals that fill an MMA stage: one warp per arrival, one A and one B group of each CTA
+  static constexpr int FULL_ARRIVALS = 2 * ((AF16 ? 0 : 4) + P_BW);
   static constexpr int OFF_BAR = OFF_RAW + RST * RSTAGE;
   static constexpr size_t SMEM = (size_t)OFF_BAR + 256 + 1024;
   static_assert(USED_COLS <= 512, "tensor memory budget");
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(SMEM > 116 * 1024, "one CTA per SM");
-  static_assert(B_TILE % 1024 == 0 && RSTAGE % 1024 == 0 && A_RAW % 1024 == 0, "stage alignment");
+  static_assert(STAGE % 1024 == 0 && RSTAGE % 1024 == 0 && A_RAW % 1024 == 0, "stage alignment");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "pair MMA N and 32-column epilogue chunks");
   static_assert(CONSUMER_WARPS % 4 == 0 && THREADS <= 1024, "warp roles");
+  static_assert(!AF16 || BBITS == 4, "fp16 activations pair with 4-bit weights");
   // A group that has finished k-block kb - n (n groups) knows that the MMAs of
   // kb - n - ST are done; its wait for the stage of kb must not pass on the
   // parity of a phase two behind, which needs n <= ST.
@@ -105,13 +118,13 @@ struct PairCfg {
   static_assert(CONSUMER_WARPS * STG_BYTES <= OFF_BAR, "epilogue staging fits in the pipeline buffers");
 };
 
-template <int BBITS, int BN, bool INTER, int ST, int RST>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST>::THREADS, 1)
+template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST, AF16>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, int M, int N, int K,
                      const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
                      uint64_t timeout_ns, int* status) {
-  using C = PairCfg<BBITS, BN, ST, RST>;
+  using C = PairCfg<BBITS, BN, ST, RST, AF16>;
   extern __shared__ uint8_t smem_raw[];
   // same offset in both CTAs: the pair MMA addresses the peer's tile by this CTA's offsets
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -120,7 +133,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
   uint64_t* rfull_bar = empty_bar + ST;                                  // raw stage landed
   uint64_t* rempty_bar = rfull_bar + RST;                                // raw stage read
   uint64_t* accum_bar = rempty_bar + RST;                                // all MMAs done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
+  uint64_t* afull_bar = accum_bar + 1;                                   // fp16 activation tile landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(afull_bar + ST);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -132,8 +146,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
-      mbar_init(&full_bar[s], 2 * (4 + P_BW));   // one A and one B group of each CTA fill a stage
+      mbar_init(&full_bar[s], C::FULL_ARRIVALS);
       mbar_init(&empty_bar[s], 1);
+      mbar_init(&afull_bar[s], 1);
     }
     for (int s = 0; s < RST; ++s) {
       mbar_init(&rfull_bar[s], 1);
@@ -161,21 +176,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < nkb; kb += C::RKB) {
-        const int grp = kb / C::RKB, rs = grp % RST;
-        if (!mbar_wait(&rempty_bar[rs], ((grp / RST) & 1) ^ 1, timeout_ns, status)) break;
-        uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE;
-        mbar_arrive_expect_tx(&rfull_bar[rs], C::A_RAW + C::B_RAW);
+      int issued = 0, issued_a = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (kb % C::RKB == 0) {
+          // raw stage for k-blocks [kb, kb + RKB): boxes past K read as zero
+          const int grp = kb / C::RKB, rs = grp % RST;
+          if (!mbar_wait(&rempty_bar[rs], ((grp / RST) & 1) ^ 1, timeout_ns, status)) break;
+          uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE;
+          mbar_arrive_expect_tx(&rfull_bar[rs], C::A_RAW + C::B_RAW);
+          if constexpr (!AF16) {
 #pragma unroll
-        for (int b = 0; b < C::RKB / 2; ++b)
-          tma_load_2d(raw + b * C::A_BOX, &tmap_a, (kb + 2 * b) * PK, m0, &rfull_bar[rs]);
-        tma_load_2d(raw + C::A_RAW, &tmap_b, kb * C::B_RAW_ROW, nb0, &rfull_bar[rs]);
-        issued = grp + 1;
+            for (int b = 0; b < C::RKB / 2; ++b)
+              tma_load_2d(raw + b * C::A_BOX, &tmap_a, (kb + 2 * b) * PK, m0, &rfull_bar[rs]);
+          }
+          tma_load_2d(raw + C::A_RAW, &tmap_b, kb * C::B_RAW_ROW, nb0, &rfull_bar[rs]);
+          issued = grp + 1;
+        }
+        if constexpr (AF16) {
+          // fp16 activations straight into the MMA stage, once the MMAs are done with it
+          const int s = kb % ST;
+          if (!mbar_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) break;
+          mbar_arrive_expect_tx(&afull_bar[s], C::A_TILE);
+          tma_load_2d(smem + s * C::STAGE, &tmap_a, kb * PK, m0, &afull_bar[s]);
+          issued_a = kb + 1;
+        }
       }
       // no TMA write may land after the CTA has exited
       for (int grp = issued > RST ? issued - RST : 0; grp < issued; ++grp)
         mbar_wait(&rfull_bar[grp % RST], (grp / RST) & 1, P_DRAIN_NS, status);
+      for (int kb = issued_a > ST ? issued_a - ST : 0; kb < issued_a; ++kb)
+        mbar_wait(&afull_bar[kb % ST], (kb / ST) & 1, P_DRAIN_NS, status);
     }
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
@@ -186,16 +216,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
       const uint32_t smem_base = __shfl_sync(0xffffffffu, smem_u32(smem), 0);
       const uint32_t idesc = idesc_f16_f32(2 * PM, BN);
+      // fp16 activations: k-blocks [0, kb_half) accumulate into slice 0, the rest into slice 1
+      const int kb_half = C::NACC == 2 ? (nkb + 1) / 2 : nkb;
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % ST;
         if (!__all_sync(0xffffffffu, mbar_wait_cluster(&full_bar[s], (kb / ST) & 1, timeout_ns, status))) break;
         tc_fence_after();
-        const uint32_t a_tm = tm + (uint32_t)(BN + s * C::A_COLS);
-        const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::B_TILE);
+        const int slice = kb < kb_half ? 0 : 1;
+        const bool first = kb == 0 || kb == kb_half;
+        const uint32_t d = tm + (uint32_t)(slice * BN);
+        const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::STAGE + C::A_TILE);
         if (elect_one()) {
+          if constexpr (AF16) {
+            const uint64_t adesc = smem_desc_sw128(smem_base + s * C::STAGE);
 #pragma unroll
-          for (int kk = 0; kk < PK / 16; ++kk)   // 16 k = 8 TMEM columns of A = +32 bytes of B
-            tc_mma_f16_ts_pair(tm, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < PK / 16; ++kk)   // +32 bytes along K = +2 in the address field
+              tc_mma_f16_pair(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+          } else {
+            const uint32_t a_tm = tm + (uint32_t)(C::ACC_COLS + s * C::A_COLS);
+#pragma unroll
+            for (int kk = 0; kk < PK / 16; ++kk)   // 16 k = 8 TMEM columns of A = +32 bytes of B
+              tc_mma_f16_ts_pair(d, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+          }
           tc_commit_pair(&empty_bar[s], 0x3);
         }
         __syncwarp();
@@ -206,7 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       mbar_wait(accum_bar, 0, P_DRAIN_NS, status);
     }
     __syncwarp();
-  } else if (warp < P_A_WARPS) {
+  } else if (warp < C::A_WARPS) {
     // ------------------------------------------------------------ int8 activations -> TMEM
     // A group g (warps 4g .. 4g + 3) converts the k-blocks kb = g (mod P_NA)
     const int q = warp & 3;                               // TMEM lane quadrant
@@ -238,7 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         ok = false;
         break;
       }
-      tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN + s * C::A_COLS), h);
+      tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::ACC_COLS + s * C::A_COLS), h);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -247,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
   } else {
     // ------------------------------------------------------------ weights -> fp16 smem
     // B group g (warps P_A_WARPS + g * P_BW ..) converts the k-blocks kb = g (mod P_NB)
-    const int bw = warp - P_A_WARPS;
+    const int bw = warp - C::A_WARPS;
     const int c = (bw % P_BW) * 32 + lane;                // converter thread within its group
     for (int kb = bw / P_BW; kb < nkb; kb += P_NB) {
       const int grp = kb / C::RKB, rs = grp % RST;
@@ -274,13 +316,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         ok = false;
         break;
       }
-      uint8_t* tb = smem + s * C::B_TILE;
+      uint8_t* tb = smem + s * C::STAGE + C::A_TILE;
 #pragma unroll
       for (int i = 0; i < C::NPB; ++i) {
         const int pi = c + i * P_B_THREADS;
         if (pi < C::B_PIECES) convert_b_piece<BBITS, INTER>(tb, pi % C::HB, pi / C::HB, v[i]);
       }
       fence_proxy_async_smem();   // generic stores -> visible to the tensor core (async proxy)
+      // fp16 activations: this CTA's half of the stage is complete once its tile has landed
+      if (AF16 && !warp_wait(&afull_bar[s], (kb / ST) & 1, timeout_ns, status)) {
+        ok = false;
+        break;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&full_bar[s]), 0));
     }
@@ -310,6 +357,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
         tmem_ld_wait();
+        if constexpr (C::NACC == 2) {
+          uint32_t r2[32];
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(col + BN), r2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+        }
         if (lane == 0) bulk_wait_read_all();   // the previous box has left the staging buffer
         __syncwarp();
         if (epi == EPI_I32) {
@@ -365,14 +419,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-template <int BBITS, int BN, bool INTER, int ST, int RST>
+template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16>
 cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
-  using C = PairCfg<BBITS, BN, ST, RST>;
+  using C = PairCfg<BBITS, BN, ST, RST, AF16>;
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
   CUtensorMap ma, mb, mc;
-  e = make_map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, 2 * PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (AF16)   // one k-block of fp16 rows: 128 bytes, the MMA's 128B swizzle
+    e = make_map(&ma, g.a, 2, (uint64_t)g.K, (uint64_t)g.M, PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
+  else        // two k-blocks of int8 rows
+    e = make_map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, 2 * PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_BOX_X, C::HB,
                C::B_BOX_X == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
@@ -383,7 +440,7 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   else
     e = make_map(&mc, g.c, 2, (uint64_t)g.N, (uint64_t)g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST>;
+  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, AF16>;
   e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(2 * ((g.M + 2 * PM - 1) / (2 * PM))), (unsigned)((g.N + BN - 1) / BN));
@@ -394,10 +451,19 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int BBITS, int BN, int ST, int RST>
+template <int BBITS, int BN, int ST, int RST, bool AF16 = false>
 cudaError_t launch_pair_layout(const GemmArgs& g, cudaStream_t stream) {
-  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_pair_t<BBITS, BN, false, ST, RST>(g, stream);
-  return launch_pair_t<BBITS, BN, true, ST, RST>(g, stream);
+  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_pair_t<BBITS, BN, false, ST, RST, AF16>(g, stream);
+  return launch_pair_t<BBITS, BN, true, ST, RST, AF16>(g, stream);
+}
+
+cudaError_t launch_pair_f16(const GemmArgs& g, int bn, cudaStream_t stream) {
+  switch (bn) {
+    case 256: return launch_pair_layout<4, 256, 4, 3, true>(g, stream);
+    case 224: return launch_pair_layout<4, 224, 4, 3, true>(g, stream);
+    case 192: return launch_pair_layout<4, 192, 4, 3, true>(g, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int BBITS>
@@ -414,7 +480,9 @@ cudaError_t launch_pair_bits(const GemmArgs& g, int bn, cudaStream_t stream) {
 }  // namespace
 
 int gemm_pair_bn(const GemmArgs& g) {
-  if (g.act != ACT_I8 || g.M <= 0 || g.N <= 0 || g.K < PK) return 0;
+  if (g.M <= 0 || g.N <= 0 || g.K < PK) return 0;
+  // fp16 activations accumulate two halves of K separately: at least two k-blocks
+  if (g.act == ACT_F16 && (g.bbits != 4 || g.K < 2 * PK)) return 0;
   // int32 outputs with int8 weights accumulate exactly in one fp32 chain only up to K = 1024
   if (g.bbits == 8 && g.epi == EPI_I32 && g.K > 1024) return 0;
   if (g.bbits != 8 && g.bbits != 4 && g.bbits != 2) return 0;
@@ -438,6 +506,7 @@ int gemm_pair_bn(const GemmArgs& g) {
 }
 
 cudaError_t launch_gemm_pair(const GemmArgs& g, int bn, cudaStream_t stream) {
+  if (g.act == ACT_F16) return launch_pair_f16(g, bn, stream);
   if (g.bbits == 4) return launch_pair_bits<4>(g, bn, stream);
   if (g.bbits == 2) return launch_pair_bits<2>(g, bn, stream);
   if (g.bbits == 8) return launch_pair_bits<8>(g, bn, stream);

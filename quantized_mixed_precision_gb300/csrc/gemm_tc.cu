@@ -291,12 +291,18 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
     const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
     const uint32_t smem_base = __shfl_sync(0xffffffffu, smem_u32(smem), 0);
     const uint32_t idesc = idesc_f16_f32(BM, BN);
+    // accumulator slice j takes the k-blocks [ceil(j nkb / NACC), ceil((j + 1) nkb / NACC))
+    int slice = 0, next_b = NACC > 1 ? (nkb + NACC - 1) / NACC : nkb;
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % ST;
       if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], (kb / ST) & 1, timeout_ns, status))) break;
       tc_fence_after();
-      const int slice = (int)(((long long)kb * NACC) / nkb);
-      const bool first = kb == 0 || slice != (int)(((long long)(kb - 1) * NACC) / nkb);
+      bool first = kb == 0;
+      while (kb == next_b && slice + 1 < NACC) {
+        ++slice;
+        first = true;
+        next_b = ((slice + 1) * nkb + NACC - 1) / NACC;
+      }
       const uint32_t d = tm + (uint32_t)(slice * BN);
       const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::STAGE + C::A_TILE);
       if (elect_one()) {
