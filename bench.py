@@ -151,16 +151,26 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+def flush_l2(flush):
+    """Write one buffer larger than L2, then read another one: the write evicts
+    whatever the previous step left in L2, and the read evicts (writes back)
+    the dirty lines of that write, so the timed step starts from a cold L2
+    without paying for someone else's write-backs."""
+    w, r = flush
+    w.zero_()
+    r.max()
+
+
 def time_steps(torch, fn, steps, warmup, flush, stream):
     """Per-step device time (ms) with CUDA events on the launching stream; L2
     flushed before every step, outside the events."""
     for _ in range(warmup):
-        flush.zero_()
+        flush_l2(flush)
         fn()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for s, e in evs:
-        flush.zero_()
+        flush_l2(flush)
         s.record(stream)
         fn()
         e.record(stream)
@@ -210,7 +220,8 @@ def run_gpu(args, rank, world, local_rank):
         dist.init_process_group("nccl")
 
     stream = torch.cuda.current_stream()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev),
+             torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=dev))
 
     # ---- headline workload: INT8 x INT4 4096^3 with per-column dequant ----
     d = W.cfg2()

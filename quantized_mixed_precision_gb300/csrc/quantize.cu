@@ -11,6 +11,7 @@
 
 #include "bq_device.cuh"
 #include "bq_internal.h"
+#include "gemm_common.cuh"
 
 namespace bq {
 
@@ -18,24 +19,41 @@ namespace {
 
 __device__ __forceinline__ int qmax_of(int bits) { return bits == 8 ? 127 : (bits == 4 ? 7 : 1); }
 
+constexpr float RNE_MAGIC = 12582912.0f;   // 1.5 * 2**23: adding it rounds |t| < 2**22 to an integer (ties to even)
+
 // Code for one element from the stored fp16 scale s (as float) and its
-// reciprocal rcp = RN(1 / s) (0 when s == 0, which yields code 0).  In F32DIV
-// mode the code is rne(RN(x / s)).  RN(x * rcp) differs from RN(x / s) by
-// less than 2**-14 for |x / s| < 256, so both round to the same integer
-// unless the product lies within 2**-12 of a half-integer; only then is the
-// IEEE division evaluated.
-__device__ __forceinline__ int quant_one(float x, float s, float rcp, int d, int mode) {
-  float r;
-  if (mode == BQ_ROUND_BMINF_HALF) {
-    r = s == 0.0f ? 0.0f : rintf(__half2float(__float2half_rn(__fdiv_rn(x, s))));
-  } else {
-    const float t = __fmul_rn(x, rcp);
-    r = rintf(t);                                     // nearest integer, ties to even
-    if (fabsf(t - r) > 0.5f - 2.44140625e-4f) r = rintf(__fdiv_rn(x, s));
-  }
-  const int q = __float2int_rn(r);
-  return q > d ? d : (q < -d ? -d : q);
+// reciprocal rcp = RN(1 / s) (0 when s == 0, which yields code 0), returned
+// as a float that carries the code in its low byte (two's complement).  In
+// F32DIV mode the code is rne(RN(x / s)) clamped to [-d, d].  RN(x * rcp)
+// differs from RN(x / s) by less than 2**-14 for |x / s| < 256, so both round
+// to the same integer unless the product lies within 2**-12 of a
+// half-integer; only then is the IEEE division evaluated.  The rounding is
+// t + 1.5 * 2**23 in fp32 (round to nearest even), whose low mantissa bits are
+// then the integer, so no float -> int conversion is needed; clamping before
+// the rounding equals clamping after it, the bounds being integers.
+__device__ __forceinline__ float code_exact(float x, float s, float fd, int mode) {
+  float t = s == 0.0f ? 0.0f : __fdiv_rn(x, s);
+  if (mode == BQ_ROUND_BMINF_HALF) t = __half2float(__float2half_rn(t));
+  return __fadd_rn(fminf(fmaxf(t, -fd), fd), RNE_MAGIC);
 }
+
+// Fast form for F32DIV: the code of x, and whether the product was too close
+// to a half-integer for it to be trusted (then code_exact decides).
+__device__ __forceinline__ float code_fast(float x, float rcp, float fd, bool& unsure) {
+  const float tc = fminf(fmaxf(__fmul_rn(x, rcp), -fd), fd);
+  const float m = __fadd_rn(tc, RNE_MAGIC);
+  unsure = fabsf(tc - __fsub_rn(m, RNE_MAGIC)) > 0.5f - 2.44140625e-4f;
+  return m;
+}
+
+__device__ __forceinline__ float quant_one(float x, float s, float rcp, float fd, int mode) {
+  if (mode == BQ_ROUND_BMINF_HALF) return code_exact(x, s, fd, mode);
+  bool unsure;
+  const float m = code_fast(x, rcp, fd, unsure);
+  return unsure ? code_exact(x, s, fd, mode) : m;
+}
+
+__device__ __forceinline__ uint32_t code_byte(float m) { return __float_as_uint(m); }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -43,65 +61,108 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// One 128-thread block per row; the row (fp16, cols % 8 == 0,
-// cols <= 1024 * VPT) lives in registers as VPT 16-byte vectors per thread,
-// so x is read from HBM exactly once.
+// fp16 rows with cols % 8 == 0 and cols <= 1024 * VPT: 128-thread blocks walk
+// the rows b, b + gridDim.x, ...; a row lives in registers as VPT 16-byte
+// vectors per thread (x is read from HBM exactly once), and the next row's
+// loads are issued before the current row is reduced and coded, so the
+// arithmetic of one row overlaps the memory latency of the next.
 constexpr int QT = 128;
+constexpr int Q_BLOCKS_PER_SM = 8;
 
-template <int VPT>
-__global__ void __launch_bounds__(QT) quantize_rows_f16_kernel(const __half* __restrict__ x, int64_t rows,
-                                                               int64_t cols, int64_t ld_x, int bits, int mode,
-                                                               int8_t* __restrict__ q, __half* __restrict__ scale) {
-  __shared__ float red[QT / 32];
+template <int VPT, int MODE>
+__global__ void __launch_bounds__(QT, Q_BLOCKS_PER_SM) quantize_rows_f16_kernel(const __half* __restrict__ x,
+                                                                                int64_t rows, int64_t cols,
+                                                                                int64_t ld_x, int bits,
+                                                                                int8_t* __restrict__ q,
+                                                                                __half* __restrict__ scale) {
+  __shared__ float red[2][QT / 32];
   const int tid = threadIdx.x;
-  const int64_t row = blockIdx.x;
   const int nvec = (int)(cols >> 3);
-  const uint4* xr = reinterpret_cast<const uint4*>(x + row * ld_x);
-  uint4 v[VPT];
-#pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int idx = tid + QT * i;
-    v[i] = idx < nvec ? __ldcs(xr + idx) : make_uint4(0, 0, 0, 0);   // streamed once
-  }
-  // |x| and max are exact in fp16: reduce packed pairs, convert once
-  __half2 m2 = __float2half2_rn(0.0f);
-#pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) m2 = __hmax2(m2, __habs2(h[j]));
-  }
-  float amax = fmaxf(__low2float(m2), __high2float(m2));
-  amax = warp_max(amax);
-  if ((tid & 31) == 0) red[tid >> 5] = amax;
-  __syncthreads();
-#pragma unroll
-  for (int w = 0; w < QT / 32; ++w) amax = fmaxf(amax, red[w]);
   const int d = qmax_of(bits);
-  const __half sh = __float2half_rn(__fdiv_rn(amax, (float)d));
-  const float s = __half2float(sh);
-  const float rcp = s == 0.0f ? 0.0f : __frcp_rn(s);
-  if (tid == 0) scale[row] = sh;
-  uint2* qr = reinterpret_cast<uint2*>(q + row * cols);
+  const float fd = (float)d;
+  int64_t row = blockIdx.x;
+  if (row >= rows) return;
+  uint4 v[VPT], vn[VPT];
+  {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * ld_x);
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int idx = tid + QT * i;
-    if (idx < nvec) {
-      const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
-      uint32_t packed[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float2 f0 = __half22float2(h[2 * j]);
-        const float2 f1 = __half22float2(h[2 * j + 1]);
-        const uint32_t b0 = (uint32_t)quant_one(f0.x, s, rcp, d, mode);
-        const uint32_t b1 = (uint32_t)quant_one(f0.y, s, rcp, d, mode);
-        const uint32_t b2 = (uint32_t)quant_one(f1.x, s, rcp, d, mode);
-        const uint32_t b3 = (uint32_t)quant_one(f1.y, s, rcp, d, mode);
-        // low bytes of the four codes -> one word
-        packed[j] = __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
-      }
-      __stcs(qr + idx, make_uint2(packed[0], packed[1]));
+    for (int i = 0; i < VPT; ++i) {
+      const int idx = tid + QT * i;
+      v[i] = idx < nvec ? __ldcs(xr + idx) : make_uint4(0, 0, 0, 0);   // streamed once
     }
+  }
+#pragma unroll 1
+  for (int it = 0; row < rows; row += gridDim.x, ++it) {
+    const int64_t nrow = row + gridDim.x;
+    if (nrow < rows) {
+      const uint4* xn = reinterpret_cast<const uint4*>(x + nrow * ld_x);
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int idx = tid + QT * i;
+        vn[i] = idx < nvec ? __ldcs(xn + idx) : make_uint4(0, 0, 0, 0);
+      }
+    }
+    // |x| and max are exact in fp16: reduce packed pairs, convert once
+    __half2 m2 = __float2half2_rn(0.0f);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m2 = __hmax2(m2, __habs2(h[j]));
+    }
+    float amax = fmaxf(__low2float(m2), __high2float(m2));
+    amax = warp_max(amax);
+    float* rb = red[it & 1];   // alternate buffers: one barrier per row suffices
+    if ((tid & 31) == 0) rb[tid >> 5] = amax;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < QT / 32; ++w) amax = fmaxf(amax, rb[w]);
+    const __half sh = __float2half_rn(__fdiv_rn(amax, fd));
+    const float s = __half2float(sh);
+    const float rcp = s == 0.0f ? 0.0f : __frcp_rn(s);
+    const bool normal_scale = s >= 6.103515625e-05f;   // 2**-14, the smallest normal fp16
+    if (tid == 0) scale[row] = sh;
+    uint2* qr = reinterpret_cast<uint2*>(q + row * cols);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int idx = tid + QT * i;
+      if (idx < nvec) {
+        const __half2* h = reinterpret_cast<const __half2*>(&v[i]);
+        float f[8], m[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 p = __half22float2(h[j]);
+          f[2 * j] = p.x;
+          f[2 * j + 1] = p.y;
+        }
+        if (MODE == BQ_ROUND_F32DIV && normal_scale) {
+          // |x / s| <= d (1 + 2**-11) for a normal scale, so no code needs clamping
+          float dev = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float t = __fmul_rn(f[e], rcp);
+            m[e] = __fadd_rn(t, RNE_MAGIC);
+            dev = fmaxf(dev, fabsf(t - __fsub_rn(m[e], RNE_MAGIC)));
+          }
+          if (dev > 0.5f - 2.44140625e-4f) {   // rare: a product within 2**-12 of a half-integer
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m[e] = quant_one(f[e], s, rcp, fd, MODE);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m[e] = quant_one(f[e], s, rcp, fd, MODE);
+        }
+        // low bytes of the codes -> two words
+        uint32_t packed[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          packed[j] = __byte_perm(__byte_perm(code_byte(m[4 * j]), code_byte(m[4 * j + 1]), 0x0040),
+                                  __byte_perm(code_byte(m[4 * j + 2]), code_byte(m[4 * j + 3]), 0x0040), 0x5410);
+        __stcs(qr + idx, make_uint2(packed[0], packed[1]));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) v[i] = vn[i];
   }
 }
 
@@ -146,14 +207,20 @@ __global__ void __launch_bounds__(256) quantize_rows_generic_kernel(const T* __r
   if (threadIdx.x == 0) scale[row] = sh;
   int8_t* qr = q + row * cols;
   for (int64_t c = threadIdx.x; c < cols; c += blockDim.x)
-    qr[c] = (int8_t)quant_one(load_as_float(xr + c), s, rcp, d, mode);
+    qr[c] = (int8_t)(uint8_t)(code_byte(quant_one(load_as_float(xr + c), s, rcp, (float)d, mode)) & 0xffu);
 }
 
 template <int VPT>
 cudaError_t launch_rows_f16(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int bits, int mode, int8_t* q,
                             uint16_t* scale, cudaStream_t stream) {
-  quantize_rows_f16_kernel<VPT><<<(unsigned)rows, QT, 0, stream>>>(
-      static_cast<const __half*>(x), rows, cols, ld_x, bits, mode, q, reinterpret_cast<__half*>(scale));
+  const int64_t blocks = (int64_t)sm_count() * Q_BLOCKS_PER_SM;
+  const unsigned grid = (unsigned)(rows < blocks ? rows : blocks);
+  if (mode == BQ_ROUND_BMINF_HALF)
+    quantize_rows_f16_kernel<VPT, BQ_ROUND_BMINF_HALF><<<grid, QT, 0, stream>>>(
+        static_cast<const __half*>(x), rows, cols, ld_x, bits, q, reinterpret_cast<__half*>(scale));
+  else
+    quantize_rows_f16_kernel<VPT, BQ_ROUND_F32DIV><<<grid, QT, 0, stream>>>(
+        static_cast<const __half*>(x), rows, cols, ld_x, bits, q, reinterpret_cast<__half*>(scale));
   return cudaGetLastError();
 }
 
