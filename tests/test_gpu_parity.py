@@ -155,6 +155,27 @@ def test_int_gemm_parity(M, N, K, bits, epi):
             assert_f16_close(y, O.dequant(c_ref, sw, sx), s_ij, f"rowcol {layout}")
 
 
+@pytest.mark.parametrize("bits", [8, 4, 2])
+@pytest.mark.parametrize("M,N,K", [(2100, 4160, 512), (2048, 4096, 576)])
+def test_int_gemm_many_tiles(M, N, K, bits):
+    """Grids of more output tiles than the GPU holds at once (several waves of
+    CTA pairs), ragged in M and N, with K a whole number of raw stages (512)
+    and not (576)."""
+    rng = np.random.default_rng(M + N + K + bits)
+    A = W.int8_uniform(rng, (M, K))
+    Bq = _codes(rng, bits, (N, K))
+    sw = W.uniform_f16(rng, (N,), 1e-3, 1e-2)
+    sx = W.uniform_f16(rng, (M,), 1e-3, 1e-1)
+    c_ref = O.gemm_int(A, Bq)
+    for layout in (["interleaved", "plain"] if bits != 8 else ["plain"]):
+        c = host(_run_int_gemm(bits, A, Bq, layout, None, None))
+        assert (c == c_ref).all(), f"int32 {layout}"
+        y = host(_run_int_gemm(bits, A, Bq, layout, dev(sx), dev(sw)))
+        s_ij = sx[:, None].astype(np.float64) * sw[None, :].astype(np.float64)
+        assert_f16_close(y, O.dequant(c_ref, sw, sx), s_ij, f"rowcol {layout}")
+    assert bq.bq_device_status(reset=True) == bq.BQ_OK
+
+
 @pytest.mark.parametrize("M", [1, 40, 200])
 def test_int_gemm_extreme_values_exact(M):
     # Largest magnitudes: -128 * -8 (4-bit, K = 16384) and -128 * -128 (int8,
