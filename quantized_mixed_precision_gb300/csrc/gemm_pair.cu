@@ -22,7 +22,7 @@
 //   P_NA groups of 4 warps    A: int8 activation row (thread = row = TMEM
 //                             lane) -> 32 fp16 pairs -> tcgen05.st into a
 //                             TMEM stage.
-//   P_NB groups of P_BW warps B: raw weight codes -> fp16 128B-swizzled
+//   NB groups of P_BW warps   B: raw weight codes -> fp16 128B-swizzled
 //                             K-major tile in shared memory.
 //   next warp                 allocates tensor memory (collectively with the
 //                             peer CTA); in the even CTA one elected lane
@@ -56,8 +56,9 @@ namespace {
 constexpr int PM = 128;                  // tile rows per CTA (256 per pair)
 constexpr int PK = 64;                   // k per block: one 128-byte fp16 swizzle row
 constexpr int P_NA = 2;                  // activation converter groups (4 warps each)
-constexpr int P_NB = 4;                  // weight converter groups
-constexpr int P_BW = 4;                  // warps per weight converter group
+constexpr int P_NB_I8 = 6;               // weight converter groups, int8 activations
+constexpr int P_NB_F16 = 6;              // weight converter groups, fp16 activations
+constexpr int P_BW = 2;                  // warps per weight converter group
 constexpr int P_A_WARPS = 4 * P_NA;
 constexpr int P_B_THREADS = P_BW * 32;   // weight converters per group
 constexpr uint64_t P_DRAIN_NS = 4000000000ull;
@@ -71,7 +72,8 @@ struct PairCfg {
   static constexpr int HB = BN / 2;                            // weight rows per CTA
   static constexpr int A_WARPS = AF16 ? 0 : P_A_WARPS;
   static constexpr int NA = AF16 ? 0 : P_NA;                   // activation converter groups
-  static constexpr int CONSUMER_WARPS = A_WARPS + P_NB * P_BW;
+  static constexpr int NB = AF16 ? P_NB_F16 : P_NB_I8;        // weight converter groups
+  static constexpr int CONSUMER_WARPS = A_WARPS + NB * P_BW;
   static constexpr int MMA_WARP = CONSUMER_WARPS;
   static constexpr int PRODUCER_WARP = MMA_WARP + 1;
   static constexpr int THREADS = (PRODUCER_WARP + 1) * 32;
@@ -99,7 +101,7 @@ struct PairCfg {
   // threads that read one (full) raw stage: a stage of RKB k-blocks is read by
   // min(groups, RKB) groups of each kind
   static constexpr int RAW_READERS =
-      (NA < RKB ? NA : RKB) * 4 * 32 + (P_NB < RKB ? P_NB : RKB) * P_B_THREADS;
+      (NA < RKB ? NA : RKB) * 4 * 32 + (NB < RKB ? NB : RKB) * P_B_THREADS;
   // arrivals that fill an MMA stage: one warp per arrival, one A and one B group of each CTA
   static constexpr int FULL_ARRIVALS = 2 * ((AF16 ? 0 : 4) + P_BW);
   static constexpr int OFF_BAR = OFF_RAW + RST * RSTAGE;
@@ -114,7 +116,7 @@ struct PairCfg {
   // A group that has finished k-block kb - n (n groups) knows that the MMAs of
   // kb - n - ST are done; its wait for the stage of kb must not pass on the
   // parity of a phase two behind, which needs n <= ST.
-  static_assert(P_NA <= ST && P_NB <= ST, "converter groups per stage ring");
+  static_assert(P_NA <= ST && NB <= ST, "converter groups per stage ring");
   static_assert(CONSUMER_WARPS * STG_BYTES <= OFF_BAR, "epilogue staging fits in the pipeline buffers");
 };
 
@@ -288,12 +290,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
     }
   } else {
     // ------------------------------------------------------------ weights -> fp16 smem
-    // B group g (warps P_A_WARPS + g * P_BW ..) converts the k-blocks kb = g (mod P_NB)
+    // B group g (warps A_WARPS + g * P_BW ..) converts the k-blocks kb = g (mod NB)
     const int bw = warp - C::A_WARPS;
     const int c = (bw % P_BW) * 32 + lane;                // converter thread within its group
-    for (int kb = bw / P_BW; kb < nkb; kb += P_NB) {
+    for (int kb = bw / P_BW; kb < nkb; kb += C::NB) {
       const int grp = kb / C::RKB, rs = grp % RST;
-      if (kb % C::RKB < P_NB && !warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
+      if (kb % C::RKB < C::NB && !warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
         ok = false;
         break;
       }
@@ -310,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         v[i] = pi < C::B_PIECES ? *reinterpret_cast<const uint4*>(raw + r * C::B_BOX_X + (pos << 4))
                                 : make_uint4(0, 0, 0, 0);
       }
-      if ((kb % C::RKB) + P_NB >= C::RKB || kb + P_NB >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
+      if ((kb % C::RKB) + C::NB >= C::RKB || kb + C::NB >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
       const int s = kb % ST;
       if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) {
         ok = false;
@@ -459,9 +461,9 @@ cudaError_t launch_pair_layout(const GemmArgs& g, cudaStream_t stream) {
 
 cudaError_t launch_pair_f16(const GemmArgs& g, int bn, cudaStream_t stream) {
   switch (bn) {
-    case 256: return launch_pair_layout<4, 256, 4, 3, true>(g, stream);
-    case 224: return launch_pair_layout<4, 224, 4, 3, true>(g, stream);
-    case 192: return launch_pair_layout<4, 192, 4, 3, true>(g, stream);
+    case 256: return launch_pair_layout<4, 256, 6, 2, true>(g, stream);
+    case 224: return launch_pair_layout<4, 224, 6, 3, true>(g, stream);
+    case 192: return launch_pair_layout<4, 192, 6, 3, true>(g, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -470,9 +472,9 @@ template <int BBITS>
 cudaError_t launch_pair_bits(const GemmArgs& g, int bn, cudaStream_t stream) {
   constexpr int RST = BBITS == 8 ? 4 : 3;
   switch (bn) {
-    case 256: return launch_pair_layout<BBITS, 256, 4, RST>(g, stream);
-    case 224: return launch_pair_layout<BBITS, 224, 4, RST>(g, stream);
-    case 192: return launch_pair_layout<BBITS, 192, 4, RST>(g, stream);
+    case 256: return launch_pair_layout<BBITS, 256, 6, BBITS == 4 ? 2 : RST>(g, stream);
+    case 224: return launch_pair_layout<BBITS, 224, 6, RST>(g, stream);
+    case 192: return launch_pair_layout<BBITS, 192, 6, RST>(g, stream);
     default: return cudaErrorInvalidValue;
   }
 }
