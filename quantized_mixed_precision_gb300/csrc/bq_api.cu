@@ -50,6 +50,8 @@ bq_status run_gemm(GemmArgs g, void* stream) {
   if (g.act == ACT_I8 && g.bbits == 8) {
     const bool tc_ok = g.M > SKINNY_M && (g.epi != EPI_I32 || g.K <= 4096);
     e = tc_ok ? launch_gemm_tc(g, s) : launch_gemm_dp4a(g, s);
+  } else if (gemm_swap_applies(g)) {
+    e = launch_gemm_swap(g, s);
   } else if (g.M <= SKINNY_M && gemv_fits(g.M, g.K, g.bbits)) {
     e = launch_gemv_mma(g, s);
   } else {

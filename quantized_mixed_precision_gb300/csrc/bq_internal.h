@@ -62,5 +62,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream);
 // for this problem, or 0 when the single-CTA kernel is the better fit.
 int gemm_pair_bn(const GemmArgs& g);
 cudaError_t launch_gemm_pair(const GemmArgs& g, int bn, cudaStream_t stream);
+// Small-M tensor-core kernel with the weights as the MMA's A operand.
+constexpr bool SWAP_ENABLED = true;
+bool gemm_swap_applies(const GemmArgs& g);
+cudaError_t launch_gemm_swap(const GemmArgs& g, cudaStream_t stream);
 
 }  // namespace bq
