@@ -41,7 +41,6 @@ namespace {
 constexpr int SW_N = 128;                // weight rows per CTA (TMEM lanes)
 constexpr int SW_K = 64;                 // k per block
 constexpr int SW_NG = 2;                 // converter groups (4 warps each)
-constexpr int SW_TMEM_COLS = 256;        // tensor-memory columns per CTA (two CTAs fit on an SM)
 constexpr uint64_t SW_DRAIN_NS = 4000000000ull;
 // M range served here: below it the skinny kernel streams the weights faster
 // (bulk copies of whole row segments), above it the CTA-pair kernel
@@ -64,11 +63,13 @@ struct SwapCfg {
   // activation stages: their own ring, deep enough to hide the load latency
   static constexpr int SX = 32768 / X_TILE >= 16 ? 16 : (32768 / X_TILE >= 4 ? 32768 / X_TILE : 4);
   static constexpr int A_COLS = SW_K / 2;                      // TMEM columns of one weight stage
-  // TMEM weight stages: every column the accumulator leaves.  The MMAs per
-  // k-block are tiny, so the ring must span the whole latency from a
-  // converter's tcgen05.st to the MMA commit that frees the stage again.
-  static constexpr int ST = (SW_TMEM_COLS - MN) / A_COLS;
-  static constexpr int NCOLS = SW_TMEM_COLS;
+  // Two accumulator slices (the two halves of K, summed in the epilogue:
+  // shorter fp32 chains) and, in the remaining columns, the TMEM weight
+  // stages.  The MMAs per k-block are tiny, so the ring spans the whole
+  // latency from a converter's tcgen05.st to the commit that frees a stage.
+  // 256 columns (two CTAs per SM) up to MN = 64, else 512.
+  static constexpr int NCOLS = 2 * MN + 4 * A_COLS <= 256 ? 256 : 512;
+  static constexpr int ST = (NCOLS - 2 * MN) / A_COLS > 8 ? 8 : (NCOLS - 2 * MN) / A_COLS;
   static constexpr int OFF_X = RST * W_RAW;
   static constexpr int OFF_BAR = OFF_X + SX * X_TILE;
   static constexpr size_t SMEM = (size_t)OFF_BAR + 512 + 1024;
@@ -99,6 +100,9 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
   const int warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * SW_N;
   const int nkb = K / SW_K;
+  // k-blocks [0, kb_half) accumulate into slice 0, the rest into slice 1
+  const int kb_half = nkb >= 2 ? (nkb + 1) / 2 : nkb;
+  const bool two_slices = kb_half < nkb;
 
   if (tid == 0) {
     for (int s = 0; s < C::ST; ++s) {
@@ -172,12 +176,14 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
                                        mbar_wait(&xfull_bar[sx], (kb / C::SX) & 1, timeout_ns, status)))
         break;
       tc_fence_after();
-      const uint32_t a_tm = tm + (uint32_t)(MN + s * C::A_COLS);
+      const uint32_t a_tm = tm + (uint32_t)(2 * MN + s * C::A_COLS);
+      const bool second = kb >= kb_half;
+      const uint32_t d = tm + (second ? (uint32_t)MN : 0u);
       const uint64_t bdesc = smem_desc_sw128(smem_base + C::OFF_X + sx * C::X_TILE);
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < SW_K / 16; ++kk)
-          tc_mma_f16_ts(tm, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16_ts(d, a_tm + 8 * kk, bdesc + 2 * kk, idesc, ((kb != 0 && kb != kb_half) || kk > 0) ? 1u : 0u);
         tc_commit(&empty_bar[s]);
         tc_commit(&xempty_bar[sx]);
       }
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
         ok = false;
         break;
       }
-      tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(MN + s * C::A_COLS), h);
+      tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(2 * MN + s * C::A_COLS), h);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -253,6 +259,13 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * c), v);
           tmem_ld_wait();
+          if (two_slices) {
+            uint32_t v2[32];
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(MN + 32 * c), v2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(v2[i]));
+          }
           if (n >= N) continue;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
