@@ -55,6 +55,25 @@ __device__ __forceinline__ float quant_one(float x, float s, float rcp, float fd
 
 __device__ __forceinline__ uint32_t code_byte(float m) { return __float_as_uint(m); }
 
+// Fast F32DIV form for two elements with packed fp32x2 arithmetic (each lane
+// of a packed op is an ordinary IEEE round-to-nearest operation): the codes
+// m = RN(x * rcp) + 1.5 * 2**23 and the distances |RN(x * rcp) - rne(.)|.
+__device__ __forceinline__ void code_fast2(float x0, float x1, float rcp, float& m0, float& m1, float& d0,
+                                           float& d1) {
+  asm("{\n\t.reg .b64 x, c, g, t, m, r, d;\n\t"
+      "mov.b64 x, {%4, %5};\n\t"
+      "mov.b64 c, {%6, %6};\n\t"
+      "mov.b64 g, {%7, %7};\n\t"
+      "mul.rn.f32x2 t, x, c;\n\t"
+      "add.rn.f32x2 m, t, g;\n\t"
+      "sub.rn.f32x2 r, m, g;\n\t"
+      "sub.rn.f32x2 d, t, r;\n\t"
+      "mov.b64 {%0, %1}, m;\n\t"
+      "mov.b64 {%2, %3}, d;\n\t}"
+      : "=f"(m0), "=f"(m1), "=f"(d0), "=f"(d1)
+      : "f"(x0), "f"(x1), "f"(rcp), "f"(RNE_MAGIC));
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -139,10 +158,10 @@ __global__ void __launch_bounds__(QT, Q_BLOCKS_PER_SM) quantize_rows_f16_kernel(
           // |x / s| <= d (1 + 2**-11) for a normal scale, so no code needs clamping
           float dev = 0.0f;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float t = __fmul_rn(f[e], rcp);
-            m[e] = __fadd_rn(t, RNE_MAGIC);
-            dev = fmaxf(dev, fabsf(t - __fsub_rn(m[e], RNE_MAGIC)));
+          for (int e = 0; e < 8; e += 2) {
+            float d0, d1;
+            code_fast2(f[e], f[e + 1], rcp, m[e], m[e + 1], d0, d1);
+            dev = fmaxf(dev, fmaxf(fabsf(d0), fabsf(d1)));
           }
           if (dev > 0.5f - 2.44140625e-4f) {   // rare: a product within 2**-12 of a half-integer
 #pragma unroll
