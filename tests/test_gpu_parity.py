@@ -225,6 +225,21 @@ def test_f16xi4_parity(M, N, K, layout):
     assert_f16_close(y, O.gemm_f16xq(X, q, s), s[None, :].astype(np.float64), "f16xi4")
 
 
+@pytest.mark.parametrize("M,N,K", [(17, 192, 64), (33, 4160, 320), (100, 320, 1088), (128, 448, 4096)])
+@pytest.mark.parametrize("layout", ["interleaved", "plain"])
+def test_f16xi4_small_m_parity(M, N, K, layout):
+    """16 < M <= 128 (weights as the MMA's A operand): a single k-block, K
+    with a ragged last raw stage, N not a multiple of the 128 weight rows of
+    a block, and M not a multiple of 16."""
+    rng = np.random.default_rng(7 * M + N + K)
+    X = W.normal_f16(rng, (M, K), 1.0)
+    q = W.int4_uniform(rng, (N, K))
+    s = W.uniform_f16(rng, (N,), 0.008, 0.016)
+    y = host(bq.bq_gemm_f16xi4(dev(X), dev(O.pack(q, 4, layout)), dev(s), layout))
+    assert_f16_close(y, O.gemm_f16xq(X, q, s), s[None, :].astype(np.float64), "f16xi4 small M")
+    assert bq.bq_device_status(reset=True) == bq.BQ_OK
+
+
 # ---------------------------------------------------------------------------
 # the five workloads at full size (sampled outputs where the oracle would be slow)
 # ---------------------------------------------------------------------------
