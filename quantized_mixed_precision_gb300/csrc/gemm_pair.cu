@@ -464,6 +464,7 @@ cudaError_t launch_pair_f16(const GemmArgs& g, int bn, cudaStream_t stream) {
     case 256: return launch_pair_layout<4, 256, 6, 2, true>(g, stream);
     case 224: return launch_pair_layout<4, 224, 6, 3, true>(g, stream);
     case 192: return launch_pair_layout<4, 192, 6, 3, true>(g, stream);
+    case 160: return launch_pair_layout<4, 160, 6, 3, true>(g, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -475,6 +476,7 @@ cudaError_t launch_pair_bits(const GemmArgs& g, int bn, cudaStream_t stream) {
     case 256: return launch_pair_layout<BBITS, 256, 6, BBITS == 4 ? 2 : RST>(g, stream);
     case 224: return launch_pair_layout<BBITS, 224, 6, RST>(g, stream);
     case 192: return launch_pair_layout<BBITS, 192, 6, RST>(g, stream);
+    case 160: return launch_pair_layout<BBITS, 160, 6, RST>(g, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -496,7 +498,7 @@ int gemm_pair_bn(const GemmArgs& g) {
   const long long mp = (g.M + 2 * PM - 1) / (2 * PM);
   int best = 0;
   long long best_cost = 0;
-  for (int bn : {256, 224, 192}) {
+  for (int bn : {256, 224, 192, 160}) {
     const long long waves = (mp * ((g.N + bn - 1) / bn) + pairs - 1) / pairs;
     const long long cost = waves * (bn + 32);
     if (best == 0 || cost < best_cost) {
