@@ -135,7 +135,9 @@ bq_status bq_pack_weights(const int8_t* q, int64_t n, int64_t k, int bits, int l
  *   for i8xi2 |a * b| <= 256 and K <= 65536 already guarantees that).
  *   With K == 0 the output is all zeros and A / B may be NULL.
  *   Any M >= 0.  Dispatch: M <= 16 runs the skinny kernel (one pass over the
- *   weights), larger M the tensor-core GEMM.
+ *   weights; int8 x int8 uses an exact dp4a kernel there), larger M the
+ *   tensor-core GEMM: 256-row tiles on CTA pairs when the grid fills the GPU,
+ *   128-row tiles with K split over a cluster otherwise.
  *   Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA.
  */
 bq_status bq_gemm_i8xi8(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
@@ -160,14 +162,17 @@ bq_status bq_gemm_i8xi2(const int8_t* A, const uint8_t* Bp, int layout, int64_t 
  *   col_scale  device fp16 (N), required
  *   Y          device fp16 (M, N)
  *   Limits: K % 64 == 0, N % 64 == 0, K <= 65536 (UNSUPPORTED otherwise).
+ *   Dispatch: M <= 16 runs the skinny kernel, 16 < M <= 128 a tensor-core
+ *   kernel with the weights as the MMA's A operand, larger M the tensor-core
+ *   GEMM on CTA pairs (or with K split over a cluster for small grids).
  *   Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA.
  */
 bq_status bq_gemm_f16xi4(const uint16_t* X, const uint8_t* Wp, int layout, int64_t M, int64_t N,
                          int64_t K, const uint16_t* col_scale, uint16_t* Y, void* stream);
 
 /*
- * Device-side wait status.  Every wait inside the tensor-core GEMM (on a
- * shared-memory mbarrier) is bounded in time.  A wait that gives up records
+ * Device-side wait status.  Every wait inside the tensor-core kernels and the
+ * skinny kernel (on a shared-memory mbarrier) is bounded in time.  A wait that gives up records
  * BQ_ERR_TIMEOUT in a device status word, abandons the tile, waits (again
  * bounded) for the tensor-core work it issued, frees its tensor memory and
  * returns, leaving the CUDA context usable.  The launch itself still
