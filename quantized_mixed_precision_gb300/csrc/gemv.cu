@@ -250,13 +250,25 @@ __host__ __device__ constexpr int gemv_bulk_smem(int K) {
   return 16 * (K * BBITS / 8 + WROW_PAD);
 }
 
-// 8 activation values (k0 .. k0+7) of one row (row pointer xr) as 4 fp16x2 words.
+// Activation bytes of all M rows (staged in shared memory when at most GEMV_XS_MAX).
 template <int ACT>
+constexpr int gemv_x_bytes(int64_t M, int64_t K) {
+  return (int)(M * K * (ACT == ACT_F16 ? 2 : 1));
+}
+
+// Largest activation block (all M rows) staged in shared memory next to the
+// weights; beyond it the activations are read from global memory.
+constexpr int GEMV_XS_MAX = 8 * 1024;
+
+// 8 activation values (k0 .. k0+7) of one row (row pointer xr, in shared
+// memory when XS, else global) as 4 fp16x2 words.
+template <int ACT, bool XS>
 __device__ __forceinline__ uint4 load_x8(const uint8_t* xr, int k0) {
   if constexpr (ACT == ACT_F16) {
+    if constexpr (XS) return *reinterpret_cast<const uint4*>(xr + 2 * k0);
     return __ldg(reinterpret_cast<const uint4*>(xr + 2 * k0));
   } else {
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(xr + k0));
+    const uint2 raw = XS ? *reinterpret_cast<const uint2*>(xr + k0) : __ldg(reinterpret_cast<const uint2*>(xr + k0));
     uint4 v;
     cvt_i8x4_f16(raw.x, v.x, v.y);
     cvt_i8x4_f16(raw.y, v.z, v.w);
@@ -265,7 +277,11 @@ __device__ __forceinline__ uint4 load_x8(const uint8_t* xr, int k0) {
 }
 
 // FULL: K is a multiple of the step, so no thread ever reaches past K.
-template <int BBITS, int ACT, int NB, bool INTER, bool FULL>
+// XS: the activations (M * K elements, at most GEMV_XS_MAX bytes) are staged
+// in shared memory after the weights: each warp copies its K range of every
+// row once (one bulk copy per row), instead of every warp of every SM
+// re-reading the same few L2 lines at each step.
+template <int BBITS, int ACT, int NB, bool INTER, bool FULL, bool XS>
 __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* __restrict__ act,
                                                                     const uint8_t* __restrict__ w, int M, int N, int K,
                                                                     const __half* __restrict__ row_scale,
@@ -275,7 +291,9 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   using C = GemvCfg<BBITS>;
   __shared__ float red[GEMV_WARPS][NB][4][32];
   __shared__ __align__(8) uint64_t wbar[GEMV_WARPS];
-  extern __shared__ __align__(16) uint8_t wsm[];         // 16 staged weight rows
+  __shared__ __align__(8) uint64_t xbar[GEMV_WARPS];
+  extern __shared__ __align__(16) uint8_t wsm[];         // 16 staged weight rows, then (XS) the activations
+  constexpr int XB = ACT == ACT_F16 ? 2 : 1;             // activation bytes per element
   const int rb = K * BBITS / 8;                          // packed bytes per weight row
   const int ws = rb + WROW_PAD;
   const int n0 = blockIdx.x * 16;
@@ -287,8 +305,13 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   const int seg_off = s_begin * STEP_W;
   const int seg = min((s_end - s_begin) * STEP_W, rb - seg_off);   // this warp's bytes per row
 
+  // this warp's activation bytes of each row: [x0, x1)
+  const int x0 = s_begin * C::STEP * XB, x1 = min(s_end * C::STEP, K) * XB;
+  uint8_t* const xsm = wsm + 16 * ws;
+
   if (lane == 0) {
     mbar_init(&wbar[warp], 1);
+    if (XS) mbar_init(&xbar[warp], 1);
     mbar_fence_init();
   }
   __syncwarp();
@@ -303,6 +326,13 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   // kernel that produced the activations before reading them
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (XS && x1 > x0) {
+    if (lane == 0) mbar_arrive_expect_tx(&xbar[warp], (uint32_t)(M * (x1 - x0)));
+    __syncwarp();
+    if (lane < M)
+      bulk_load(xsm + (size_t)lane * K * XB + x0, static_cast<const uint8_t*>(act) + (size_t)lane * K * XB + x0,
+                (uint32_t)(x1 - x0), &xbar[warp]);
+  }
 
   // Each warp waits for its own quarter; on a timeout it still waits
   // (bounded) for its copies before it may exit, and skips the math.
@@ -310,6 +340,11 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   if (seg > 0) {
     w_ok = mbar_wait(&wbar[warp], 0, timeout_ns, status);
     if (!w_ok) mbar_wait(&wbar[warp], 0, 4000000000ull, status);
+  }
+  if (XS && x1 > x0) {
+    const bool x_ok = mbar_wait(&xbar[warp], 0, timeout_ns, status);
+    if (!x_ok) mbar_wait(&xbar[warp], 0, 4000000000ull, status);
+    w_ok = w_ok && x_ok;
   }
   w_ok = __all_sync(0xffffffffu, w_ok);
 
@@ -323,7 +358,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
     const int m = nb * 8 + g;
-    xr[nb] = static_cast<const uint8_t*>(act) + (size_t)(m < M ? m : 0) * K * (ACT == ACT_F16 ? 2 : 1);
+    xr[nb] = (XS ? xsm : static_cast<const uint8_t*>(act)) + (size_t)(m < M ? m : 0) * K * XB;
   }
 
   float d[2][NB][4];
@@ -337,15 +372,16 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
 #pragma unroll 2
   for (int s = s_begin; s < s_stop; ++s) {
     const int kbase = s * C::STEP + t * C::E16;          // first k of this thread's 16 bytes
-    // a ragged last step: threads past K read zero weights (and in-range activations)
+    // a ragged last step: threads past K read zero weights and activations
+    // of the warp's own first step (staged, finite)
     const bool kin = FULL || kbase < K;
-    const int kx = kin ? kbase : 0;
-    // activation fragments first (L1/L2 resident), overlapping the conversion
+    const int kx = kin ? kbase : s_begin * C::STEP;
+    // activation fragments first, overlapping the conversion
     uint4 xb[C::CPT][NB];
 #pragma unroll
     for (int j = 0; j < C::CPT; ++j)
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = load_x8<ACT>(xr[nb], kx + 8 * j);
+      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = load_x8<ACT, XS>(xr[nb], kx + 8 * j);
     const uint32_t woff = (uint32_t)s * STEP_W;
     uint4 va = *reinterpret_cast<const uint4*>(wr0 + (kin ? woff : 0));
     uint4 vb = *reinterpret_cast<const uint4*>(wr1 + (kin ? woff : 0));
@@ -400,13 +436,13 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   }
 }
 
-template <int BBITS, int ACT, int NB, bool INTER, bool FULL>
+template <int BBITS, int ACT, int NB, bool INTER, bool FULL, bool XS>
 cudaError_t launch_bulk(const GemmArgs& g, cudaStream_t stream) {
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
-  const int smem = gemv_bulk_smem<BBITS>((int)g.K);
-  auto kern = gemv_bulk_kernel<BBITS, ACT, NB, INTER, FULL>;
+  const int smem = gemv_bulk_smem<BBITS>((int)g.K) + (XS ? gemv_x_bytes<ACT>(g.M, g.K) : 0);
+  auto kern = gemv_bulk_kernel<BBITS, ACT, NB, INTER, FULL, XS>;
   if (smem > 48 * 1024) {
     e = set_smem_once(kern, smem);
     if (e != cudaSuccess) return e;
@@ -453,18 +489,25 @@ cudaError_t launch_bits_act(const GemmArgs& g, cudaStream_t stream) {
   const bool inter = g.layout == BQ_LAYOUT_INTERLEAVED;
   if (gemv_bulk_smem<BBITS>((int)g.K) <= 64 * 1024) {
     const bool full = g.K % GemvCfg<BBITS>::STEP == 0;
+    if (g.M <= 8 && gemv_x_bytes<ACT>(g.M, g.K) <= GEMV_XS_MAX) {
+      if (full)
+        return inter ? launch_bulk<BBITS, ACT, 1, true, true, true>(g, stream)
+                     : launch_bulk<BBITS, ACT, 1, false, true, true>(g, stream);
+      return inter ? launch_bulk<BBITS, ACT, 1, true, false, true>(g, stream)
+                   : launch_bulk<BBITS, ACT, 1, false, false, true>(g, stream);
+    }
     if (g.M <= 8) {
       if (full)
-        return inter ? launch_bulk<BBITS, ACT, 1, true, true>(g, stream)
-                     : launch_bulk<BBITS, ACT, 1, false, true>(g, stream);
-      return inter ? launch_bulk<BBITS, ACT, 1, true, false>(g, stream)
-                   : launch_bulk<BBITS, ACT, 1, false, false>(g, stream);
+        return inter ? launch_bulk<BBITS, ACT, 1, true, true, false>(g, stream)
+                     : launch_bulk<BBITS, ACT, 1, false, true, false>(g, stream);
+      return inter ? launch_bulk<BBITS, ACT, 1, true, false, false>(g, stream)
+                   : launch_bulk<BBITS, ACT, 1, false, false, false>(g, stream);
     }
     if (full)
-      return inter ? launch_bulk<BBITS, ACT, 2, true, true>(g, stream)
-                   : launch_bulk<BBITS, ACT, 2, false, true>(g, stream);
-    return inter ? launch_bulk<BBITS, ACT, 2, true, false>(g, stream)
-                 : launch_bulk<BBITS, ACT, 2, false, false>(g, stream);
+      return inter ? launch_bulk<BBITS, ACT, 2, true, true, false>(g, stream)
+                   : launch_bulk<BBITS, ACT, 2, false, true, false>(g, stream);
+    return inter ? launch_bulk<BBITS, ACT, 2, true, false, false>(g, stream)
+                 : launch_bulk<BBITS, ACT, 2, false, false, false>(g, stream);
   }
   if (g.M <= 8) return inter ? launch_t<BBITS, ACT, 1, true>(g, stream) : launch_t<BBITS, ACT, 1, false>(g, stream);
   return inter ? launch_t<BBITS, ACT, 2, true>(g, stream) : launch_t<BBITS, ACT, 2, false>(g, stream);

@@ -225,6 +225,33 @@ def test_f16xi4_parity(M, N, K, layout):
     assert_f16_close(y, O.gemm_f16xq(X, q, s), s[None, :].astype(np.float64), "f16xi4")
 
 
+@pytest.mark.parametrize("M,N,K", [(2, 320, 2048), (8, 192, 512), (3, 64, 1344), (5, 128, 832)])
+@pytest.mark.parametrize("layout", ["interleaved", "plain"])
+def test_f16xi4_skinny_staged_activations(M, N, K, layout):
+    """Skinny kernel with the activations staged in shared memory (M * K * 2
+    bytes up to 8 KB: the first three shapes, 1344 with a ragged last step)
+    and just above that limit (read from global memory)."""
+    rng = np.random.default_rng(7 * M + N + K)
+    X = W.normal_f16(rng, (M, K), 1.0)
+    q = W.int4_uniform(rng, (N, K))
+    s = W.uniform_f16(rng, (N,), 0.008, 0.016)
+    y = host(bq.bq_gemm_f16xi4(dev(X), dev(O.pack(q, 4, layout)), dev(s), layout))
+    assert_f16_close(y, O.gemm_f16xq(X, q, s), s[None, :].astype(np.float64), "f16xi4 staged")
+
+
+@pytest.mark.parametrize("bits,M,N,K", [(4, 7, 128, 1088), (2, 6, 192, 1344), (2, 1, 64, 8192), (4, 8, 64, 1024)])
+def test_int_skinny_staged_activations(bits, M, N, K):
+    """int8 activations staged in shared memory (M * K bytes up to 8 KB),
+    ragged last steps included: exact int32 results."""
+    rng = np.random.default_rng(bits * 1000 + M * 31 + K)
+    A = W.int8_uniform(rng, (M, K))
+    Bq = _codes(rng, bits, (N, K))
+    c_ref = O.gemm_int(A, Bq)
+    for layout in ("interleaved", "plain"):
+        c = host(_run_int_gemm(bits, A, Bq, layout, None, None))
+        assert (c == c_ref).all(), f"layout {layout}"
+
+
 @pytest.mark.parametrize("M,N,K", [(17, 192, 64), (33, 4160, 320), (100, 320, 1088), (128, 448, 4096)])
 @pytest.mark.parametrize("layout", ["interleaved", "plain"])
 def test_f16xi4_small_m_parity(M, N, K, layout):
