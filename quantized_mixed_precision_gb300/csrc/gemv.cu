@@ -352,12 +352,16 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   const int s_stop = w_ok ? s_end : s_begin;
   const uint8_t* wr0 = wsm + g * ws + 16 * t;
   const uint8_t* wr1 = wr0 + 8 * ws;
-  // Activation row of each MMA column: MMA columns past M read row 0 (their
-  // results are never stored), so the loads need no predicate.
+  // Activation row of each MMA column.  Lanes whose column is past M load
+  // nothing and feed zeros (those columns are never stored): with M = 1 only
+  // the 4 lanes of column 0 read activations, so a fragment load moves 64
+  // bytes through the shared-memory / L1 data path instead of 512.
   const uint8_t* xr[NB];
+  bool xv[NB];
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
     const int m = nb * 8 + g;
+    xv[nb] = m < M;
     xr[nb] = (XS ? xsm : static_cast<const uint8_t*>(act)) + (size_t)(m < M ? m : 0) * K * XB;
   }
 
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
 #pragma unroll
     for (int j = 0; j < C::CPT; ++j)
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = load_x8<ACT, XS>(xr[nb], kx + 8 * j);
+      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = xv[nb] ? load_x8<ACT, XS>(xr[nb], kx + 8 * j) : make_uint4(0, 0, 0, 0);
     const uint32_t woff = (uint32_t)s * STEP_W;
     uint4 va = *reinterpret_cast<const uint4*>(wr0 + (kin ? woff : 0));
     uint4 vb = *reinterpret_cast<const uint4*>(wr1 + (kin ? woff : 0));
