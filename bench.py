@@ -269,6 +269,23 @@ def time_graph(torch, g, reps, stream):
     return statistics.median(ts)
 
 
+def max_over_ranks(torch, values, device, world):
+    """Per-rank timings -> the slowest rank's, element by element (MAX
+    all-reduce over the default process group); unchanged for one rank."""
+    values = [float(v) for v in values]
+    if world <= 1:
+        return values
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(world, units_per_rank_step, steps, slowest_ms, scale=1e12):
+    """Units processed by all ranks (each does the same work) divided by the
+    slowest rank's time, per second, in multiples of `scale`."""
+    return world * units_per_rank_step * steps / (slowest_ms * 1e-3) / scale
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
 
@@ -325,13 +342,9 @@ def run_gpu(args, rank, world, local_rank):
             torch.distributed.barrier()
         t_wall = time.perf_counter() - t_wall0
     clocks = clk.summary()
-    total_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    (total_ms,) = max_over_ranks(torch, [e0.elapsed_time(e1)], dev, world)
     ms_step = total_ms / args.steps
-    value = world * OPS2 * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(world, OPS2, args.steps, total_ms)
     single = time_steps(torch, lambda: step(0), 5, 2, flush, stream)
     del graph, sets
 
@@ -341,12 +354,9 @@ def run_gpu(args, rank, world, local_rank):
     sc_h = torch.from_numpy(d["scale"]).pin_memory()
     h2d_bytes = A_h.numel() + Bp_h.numel() + 2 * sc_h.numel()
     d2h_bytes = 2 * M2 * N2
-    e2e_ms, e2e_serial_ms = e2e_pipelined(torch, bq, A_h, Bp_h, sc_h, dev, args.steps, args.warmup)
-    if world > 1:
-        t = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms, e2e_serial_ms = (float(x) for x in t.tolist())
-    e2e = {"value": world * OPS2 * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+    e2e_ms, e2e_serial_ms = max_over_ranks(torch, e2e_pipelined(torch, bq, A_h, Bp_h, sc_h, dev, args.steps,
+                                                                  args.warmup), dev, world)
+    e2e = {"value": whole_job_rate(world, OPS2, args.steps, e2e_ms), "unit": "TOPS",
            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": e2e_ms / args.steps,
            "method": "every step copies its A, B and scale host->device and its C device->host (pinned buffers) "
                      "around one C-ABI call; three buffer sets on three streams, so step i's GEMM overlaps step "
@@ -372,14 +382,14 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     reps = max(1, args.steps // 4)
     g3 = capture(torch, lambda: [gemv_stack() for _ in range(reps)])
-    gemv_ms = time_graph(torch, g3, 5, stream) / (reps * GEMV_LAYERS)
+    (gemv_ms,) = max_over_ranks(torch, [time_graph(torch, g3, 5, stream) / (reps * GEMV_LAYERS)], dev, world)
     gemv_single = statistics.median(time_steps(torch, lambda: bq.bq_gemm_f16xi4(X3, W3, s3, "interleaved", out=Y3[0]),
                                                args.steps, args.warmup, flush, stream))
     gemv_bytes = roofline.matmul_min_bytes(1, 4096, 11008, 16, 4, 16, extra_bytes=2 * 11008)
     gbs = gemv_bytes / (gemv_ms * 1e-3) / 1e9
     gemv = {"value": gbs, "unit": "GB/s", "ms": gemv_ms, "workload": GEMV_WORKLOAD,
             "method": f"{GEMV_LAYERS} layers with distinct weights ({GEMV_LAYERS * 22.5:.0f} MB) back to back in a "
-                      f"CUDA graph, {reps} rounds",
+                      f"CUDA graph, {reps} rounds; per GPU, the slowest rank's time",
             "single_launch_ms_l2_flushed": gemv_single,
             "single_launch_GB/s": gemv_bytes / (gemv_single * 1e-3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
