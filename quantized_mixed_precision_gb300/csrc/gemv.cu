@@ -262,13 +262,17 @@ constexpr int GEMV_XS_MAX = 8 * 1024;
 
 // 8 activation values (k0 .. k0+7) of one row (row pointer xr, in shared
 // memory when XS, else global) as 4 fp16x2 words.
+// A lane with live == false loads nothing and returns zeros (the conversion
+// runs unpredicated, so the branch covers only the load).
 template <int ACT, bool XS>
-__device__ __forceinline__ uint4 load_x8(const uint8_t* xr, int k0) {
+__device__ __forceinline__ uint4 load_x8(const uint8_t* xr, int k0, bool live) {
   if constexpr (ACT == ACT_F16) {
+    if (!live) return make_uint4(0, 0, 0, 0);
     if constexpr (XS) return *reinterpret_cast<const uint4*>(xr + 2 * k0);
     return __ldg(reinterpret_cast<const uint4*>(xr + 2 * k0));
   } else {
-    const uint2 raw = XS ? *reinterpret_cast<const uint2*>(xr + k0) : __ldg(reinterpret_cast<const uint2*>(xr + k0));
+    uint2 raw = make_uint2(0, 0);
+    if (live) raw = XS ? *reinterpret_cast<const uint2*>(xr + k0) : __ldg(reinterpret_cast<const uint2*>(xr + k0));
     uint4 v;
     cvt_i8x4_f16(raw.x, v.x, v.y);
     cvt_i8x4_f16(raw.y, v.z, v.w);
@@ -385,7 +389,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
 #pragma unroll
     for (int j = 0; j < C::CPT; ++j)
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = xv[nb] ? load_x8<ACT, XS>(xr[nb], kx + 8 * j) : make_uint4(0, 0, 0, 0);
+      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = load_x8<ACT, XS>(xr[nb], kx + 8 * j, xv[nb]);
     const uint32_t woff = (uint32_t)s * STEP_W;
     uint4 va = *reinterpret_cast<const uint4*>(wr0 + (kin ? woff : 0));
     uint4 vb = *reinterpret_cast<const uint4*>(wr1 + (kin ? woff : 0));
