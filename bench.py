@@ -451,6 +451,17 @@ def measure_paths(torch, bq, W, roofline, dev, flush, stream, hbm_peak, tc_peak,
     B0 = bq.bq_pack_weights(torch.from_numpy(d0["B"]).to(dev), 4, "plain")
     ms = med(lambda: bq.bq_gemm_i8xi4(A0, B0, "plain"))
     out["i8xi4_i32_256^3"] = {"ms": ms, "TOPS": roofline.matmul_ops(256, 256, 256) / (ms * 1e-3) / 1e12}
+    # INT8 x INT4 4096^3 with the dequantisation followed by a fused activation
+    d2 = W.cfg2()
+    A2 = torch.from_numpy(d2["A"]).to(dev)
+    B2 = bq.bq_pack_weights(torch.from_numpy(d2["B"]).to(dev), 4, "interleaved")
+    s2 = torch.from_numpy(d2["scale"]).to(dev)
+    C2 = torch.empty((4096, 4096), dtype=torch.float16, device=dev)
+    for act in ("none", "relu", "gelu"):
+        ms = med(lambda: bq.bq_gemm_i8xi4_act(A2, B2, act, "interleaved", col_scale=s2, out=C2))
+        out[f"i8xi4_{act}_4096^3"] = {"ms": ms, "TOPS": OPS2 / (ms * 1e-3) / 1e12,
+                                      "tc_frac": OPS2 / (ms * 1e-3) / 1e12 / tc_peak}
+    del A2, B2, s2, C2
     # fp16 x INT4, dynamic M
     d3 = W.cfg3(M=1024, source=False)
     W3 = bq.bq_pack_weights(torch.from_numpy(d3["W"]).to(dev), 4, "interleaved")

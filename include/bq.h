@@ -27,6 +27,11 @@
  *             fp16 scale = absmax / 127, codes = nearbyint(x / scale);
  *             elementwise_copy_scale: int32 * w_scale * x_scale -> fp16;
  *             igemm: int8 x int8 -> int32).
+ *   [Pallas]  "JAX Pallas 在 TPU 上编写高效矩阵乘法内核：从分块算法、性能建模到
+ *             算子融合", section 模板化矩阵乘法 / 融合激活函数 (the activation
+ *             acts on the f32 result of the last step, before the one downcast).
+ *   [DISC]    "全面支持 PyTorch 2.0：BladeDISC 5 月~11 月新功能发布", section
+ *             Ongoing Work / CUTLASS Gemm CodeGen (GEMM + GELU fusion).
  */
 #ifndef BQ_H_
 #define BQ_H_
@@ -50,6 +55,7 @@ typedef enum bq_status {
 typedef enum bq_ftype { BQ_F16 = 0, BQ_F32 = 1 } bq_ftype;
 typedef enum bq_layout { BQ_LAYOUT_PLAIN = 0, BQ_LAYOUT_INTERLEAVED = 1 } bq_layout;
 typedef enum bq_round { BQ_ROUND_F32DIV = 0, BQ_ROUND_BMINF_HALF = 1 } bq_round;
+typedef enum bq_activation { BQ_ACT_NONE = 0, BQ_ACT_RELU = 1, BQ_ACT_GELU = 2 } bq_activation;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* bq_status_string(int status);
@@ -169,6 +175,35 @@ bq_status bq_gemm_i8xi2(const int8_t* A, const uint8_t* Bp, int layout, int64_t 
  */
 bq_status bq_gemm_f16xi4(const uint16_t* X, const uint8_t* Wp, int layout, int64_t M, int64_t N,
                          int64_t K, const uint16_t* col_scale, uint16_t* Y, void* stream);
+
+/*
+ * GEMMs with a fused activation epilogue.  [Pallas 融合激活函数; DISC GEMM +
+ * GELU]
+ *
+ *   Same operands, limits, dispatch and errors as the call without "_act";
+ *   the output must be fp16 (col_scale required).  The activation acts on
+ *   the fp32 dequantised value v (after every scale product) and the result
+ *   is rounded once to fp16:
+ *     C[i, j] = fp16_rne( act(v[i, j]) )
+ *   activation  BQ_ACT_NONE  act(v) = v
+ *               BQ_ACT_RELU  act(v) = max(v, 0)
+ *               BQ_ACT_GELU  act(v) = v * Phi(v) = 0.5 * v * erfc(-v / sqrt(2))
+ *                            (the erf form; evaluated in fp32 with erfcf, which
+ *                            has no cancellation for negative v)
+ *   Errors: INVALID_ARG also for an unknown activation or a NULL col_scale.
+ */
+bq_status bq_gemm_i8xi8_act(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
+                            const uint16_t* row_scale, const uint16_t* col_scale, int activation,
+                            void* C, void* stream);
+bq_status bq_gemm_i8xi4_act(const int8_t* A, const uint8_t* Bp, int layout, int64_t M, int64_t N,
+                            int64_t K, const uint16_t* row_scale, const uint16_t* col_scale,
+                            int activation, void* C, void* stream);
+bq_status bq_gemm_i8xi2_act(const int8_t* A, const uint8_t* Bp, int layout, int64_t M, int64_t N,
+                            int64_t K, const uint16_t* row_scale, const uint16_t* col_scale,
+                            int activation, void* C, void* stream);
+bq_status bq_gemm_f16xi4_act(const uint16_t* X, const uint8_t* Wp, int layout, int64_t M, int64_t N,
+                             int64_t K, const uint16_t* col_scale, int activation, uint16_t* Y,
+                             void* stream);
 
 /*
  * Device-side wait status.  Every wait inside the tensor-core kernels and the

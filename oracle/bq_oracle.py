@@ -43,9 +43,20 @@ the design notes with its reason):
       overflows for |C| >= 65520; ``dequant_literal_fp16`` reports that).
 * Q11 fp16 x int4 applies the per-channel scale after an exact (float64)
       accumulation.
+* Q15 a fused activation acts on the dequantised value (after every scale
+      product, as the Pallas page applies it to the f32 result of the last
+      step before the one downcast) and the result is rounded once to fp16;
+      GELU is the erf form v * Phi(v) (the BladeDISC page names GELU without
+      a formula).
+
+A fused activation follows [Pallas] section "模板化矩阵乘法 / 融合激活函数"
+and [DISC] "全面支持 PyTorch 2.0：BladeDISC 5 月~11 月新功能发布", section
+"Ongoing Work / CUTLASS Gemm CodeGen" (GEMM + GELU).
 """
 
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -251,18 +262,37 @@ def gemm_int(a: np.ndarray, b_codes: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # a6: fused dequantisation  [BitBLAS 2. 添加反量化支持; BMINF elementwise_copy_scale]
 # ---------------------------------------------------------------------------
+def activation(v: np.ndarray, kind: str = "none") -> np.ndarray:
+    """The fused activation, in float64 (reading Q15).
+
+    "none": v;  "relu": max(v, 0);  "gelu": v * Phi(v) with Phi the standard
+    normal distribution function, Phi(v) = erfc(-v / sqrt(2)) / 2.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    if kind == "none":
+        return v
+    if kind == "relu":
+        return np.where(v > 0.0, v, 0.0)
+    if kind == "gelu":
+        phi = np.vectorize(lambda t: 0.5 * math.erfc(-t / math.sqrt(2.0)), otypes=[np.float64])
+        return v * phi(v) if v.size else v
+    raise ValueError(kind)
+
+
 def dequant(c: np.ndarray, col_scale: np.ndarray,
-            row_scale: np.ndarray | None = None) -> np.ndarray:
-    """D[i, j] = fp16( (float(C[i, j]) * float(sw[j])) * float(sx[i]) ).
+            row_scale: np.ndarray | None = None, act: str = "none") -> np.ndarray:
+    """D[i, j] = fp16( act( (float(C[i, j]) * float(sw[j])) * float(sx[i]) ) ).
 
     All products in IEEE fp32 (each rounded to nearest-even), one final
     rounding to fp16 (reading Q10).  Without a row scale the second product
-    is omitted.
+    is omitted.  The activation (reading Q15) acts on that fp32 value.
     """
     cf = np.asarray(c, dtype=np.int32).astype(np.float32)
     out = cf * col_scale.astype(np.float32)[None, :]
     if row_scale is not None:
         out = out * row_scale.astype(np.float32)[:, None]
+    if act != "none":
+        out = activation(out, act)
     with np.errstate(over="ignore"):
         return out.astype(np.float16)
 
@@ -279,17 +309,21 @@ def dequant_literal_fp16(c: np.ndarray, col_scale: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # a7 / a8: fp16 activations x 4-bit weights  [BitBLAS 案例2; 高级功能 动态形状]
 # ---------------------------------------------------------------------------
-def gemm_f16xq(x: np.ndarray, w_codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
-    """Y[i, j] = fp16( s[j] * sum_k float(X[i, k]) * q[j, k] ).
+def gemm_f16xq(x: np.ndarray, w_codes: np.ndarray, scale: np.ndarray, act: str = "none") -> np.ndarray:
+    """Y[i, j] = fp16( act( s[j] * sum_k float(X[i, k]) * q[j, k] ) ).
 
     The sum is a float64 matmul (library step).  For fp16 X and 4-bit codes
     every product needs at most 15 significant bits and the partial sums of
     K <= 2**16 terms stay inside float64's 53-bit significand, so the sum is
-    exact; the per-channel scale is applied after it (reading Q11).
+    exact; the per-channel scale is applied after it (reading Q11), then the
+    activation (reading Q15).
     """
     acc = np.asarray(x, dtype=np.float64) @ np.asarray(w_codes, dtype=np.float64).T
+    v = acc * scale.astype(np.float64)[None, :]
+    if act != "none":
+        v = activation(v, act)
     with np.errstate(over="ignore"):
-        return (acc * scale.astype(np.float64)[None, :]).astype(np.float16)
+        return v.astype(np.float16)
 
 
 def gemm_f16xq_acc(x: np.ndarray, w_codes: np.ndarray) -> np.ndarray:

@@ -23,6 +23,8 @@ BQ_F16, BQ_F32 = 0, 1
 LAYOUT_PLAIN, LAYOUT_INTERLEAVED = 0, 1
 ROUND_F32DIV, ROUND_BMINF_HALF = 0, 1
 LAYOUTS = {"plain": LAYOUT_PLAIN, "interleaved": LAYOUT_INTERLEAVED}
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "gelu": ACT_GELU}
 
 _c_i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -37,6 +39,13 @@ _SIGNATURES = {
     "bq_gemm_i8xi4": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp]),
     "bq_gemm_i8xi2": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp, _vp]),
     "bq_gemm_f16xi4": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, _vp]),
+    "bq_gemm_i8xi8_act": (ctypes.c_int, [_vp, _vp, _c_i64, _c_i64, _c_i64, _vp, _vp, ctypes.c_int, _vp, _vp]),
+    "bq_gemm_i8xi4_act": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, ctypes.c_int,
+                                         _vp, _vp]),
+    "bq_gemm_i8xi2_act": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, ctypes.c_int,
+                                         _vp, _vp]),
+    "bq_gemm_f16xi4_act": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, ctypes.c_int, _vp,
+                                          _vp]),
     "bq_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "bq_set_wait_timeout_ns": (_c_i64, [_c_i64]),
 }
@@ -116,6 +125,10 @@ def _need(t, dtype, name, ndim=None):
 
 def _layout(layout):
     return LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+
+
+def _activation(activation):
+    return ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
 
 
 # ----------------------------------------------------------------------------
@@ -220,6 +233,65 @@ def bq_gemm_f16xi4(X, Wp, col_scale, layout=LAYOUT_INTERLEAVED, out=None, stream
     st = lib().bq_gemm_f16xi4(_ptr(X), _ptr(Wp), _layout(layout), M, N, K, _ptr(col_scale), _ptr(out),
                               _stream(stream))
     _check(st, "bq_gemm_f16xi4")
+    return out
+
+
+def bq_gemm_i8xi8_act(A, B, activation, row_scale=None, col_scale=None, out=None, stream=None):
+    """int8 x int8 GEMM with the fp16 dequantisation and a fused activation ("none", "relu", "gelu")."""
+    torch = _torch()
+    _need(A, torch.int8, "A", 2)
+    _need(B, torch.int8, "B", 2)
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("K mismatch")
+    out = _gemm_out(M, N, col_scale is not None, out, A.device)
+    st = lib().bq_gemm_i8xi8_act(_ptr(A), _ptr(B), M, N, K, _ptr(row_scale), _ptr(col_scale),
+                                 _activation(activation), _ptr(out), _stream(stream))
+    _check(st, "bq_gemm_i8xi8_act")
+    return out
+
+
+def _gemm_packed_act(fn_name, bits, A, Bp, layout, activation, row_scale, col_scale, out, stream):
+    torch = _torch()
+    _need(A, torch.int8, "A", 2)
+    _need(Bp, torch.uint8, "Bp", 2)
+    M, K = A.shape
+    N = Bp.shape[0]
+    if Bp.shape[1] * 8 != K * bits:
+        raise ValueError("packed width does not match K")
+    out = _gemm_out(M, N, col_scale is not None, out, A.device)
+    st = getattr(lib(), fn_name)(_ptr(A), _ptr(Bp), _layout(layout), M, N, K, _ptr(row_scale), _ptr(col_scale),
+                                 _activation(activation), _ptr(out), _stream(stream))
+    _check(st, fn_name)
+    return out
+
+
+def bq_gemm_i8xi4_act(A, Bp, activation, layout=LAYOUT_INTERLEAVED, row_scale=None, col_scale=None, out=None,
+                      stream=None):
+    return _gemm_packed_act("bq_gemm_i8xi4_act", 4, A, Bp, layout, activation, row_scale, col_scale, out, stream)
+
+
+def bq_gemm_i8xi2_act(A, Bp, activation, layout=LAYOUT_INTERLEAVED, row_scale=None, col_scale=None, out=None,
+                      stream=None):
+    return _gemm_packed_act("bq_gemm_i8xi2_act", 2, A, Bp, layout, activation, row_scale, col_scale, out, stream)
+
+
+def bq_gemm_f16xi4_act(X, Wp, col_scale, activation, layout=LAYOUT_INTERLEAVED, out=None, stream=None):
+    torch = _torch()
+    _need(X, torch.float16, "X", 2)
+    _need(Wp, torch.uint8, "Wp", 2)
+    _need(col_scale, torch.float16, "col_scale", 1)
+    M, K = X.shape
+    N = Wp.shape[0]
+    if Wp.shape[1] * 2 != K:
+        raise ValueError("packed width does not match K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    _need(out, torch.float16, "out", 2)
+    st = lib().bq_gemm_f16xi4_act(_ptr(X), _ptr(Wp), _layout(layout), M, N, K, _ptr(col_scale),
+                                  _activation(activation), _ptr(out), _stream(stream))
+    _check(st, "bq_gemm_f16xi4_act")
     return out
 
 

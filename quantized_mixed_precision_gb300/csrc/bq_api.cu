@@ -23,6 +23,12 @@ inline bool valid_bits(int bits) { return bits == 8 || bits == 4 || bits == 2; }
 
 inline bool valid_layout(int layout) { return layout == BQ_LAYOUT_PLAIN || layout == BQ_LAYOUT_INTERLEAVED; }
 
+// An activation needs the fp16 output (col_scale given); NONE is always valid.
+inline bool valid_activation(int activation, const void* col_scale) {
+  if (activation == BQ_ACT_NONE) return true;
+  return (activation == BQ_ACT_RELU || activation == BQ_ACT_GELU) && col_scale != nullptr;
+}
+
 // Shared checks of the GEMM entry points.  max_k bounds K so that every
 // partial sum of the integer paths stays below 2**24 (exact fp32 accumulation).
 bq_status check_gemm(const void* a, const void* b, int64_t M, int64_t N, int64_t K, const void* row_scale,
@@ -135,41 +141,66 @@ bq_status bq_pack_weights(const int8_t* q, int64_t n, int64_t k, int bits, int l
 
 bq_status bq_gemm_i8xi8(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
                         const uint16_t* row_scale, const uint16_t* col_scale, void* C, void* stream) {
+  return bq_gemm_i8xi8_act(A, B, M, N, K, row_scale, col_scale, BQ_ACT_NONE, C, stream);
+}
+
+bq_status bq_gemm_i8xi8_act(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
+                            const uint16_t* row_scale, const uint16_t* col_scale, int activation, void* C,
+                            void* stream) {
+  if (!valid_activation(activation, col_scale)) return BQ_ERR_INVALID_ARG;
   bq_status st = check_gemm(A, B, M, N, K, row_scale, col_scale, C, MAX_K);
   if (st != BQ_OK) return st;
-  GemmArgs g{A, B, ACT_I8, 8, BQ_LAYOUT_PLAIN, M, N, K, row_scale, col_scale, EPI_I32, C};
+  GemmArgs g{A, B, ACT_I8, 8, BQ_LAYOUT_PLAIN, M, N, K, row_scale, col_scale, EPI_I32, C, activation};
   return run_gemm(g, stream);
 }
 
 static bq_status gemm_sub_byte(const int8_t* A, const uint8_t* Bp, int layout, int bits, int64_t M, int64_t N,
-                               int64_t K, const uint16_t* row_scale, const uint16_t* col_scale, void* C,
-                               void* stream) {
-  if (!valid_layout(layout)) return BQ_ERR_INVALID_ARG;
+                               int64_t K, const uint16_t* row_scale, const uint16_t* col_scale, int activation,
+                               void* C, void* stream) {
+  if (!valid_layout(layout) || !valid_activation(activation, col_scale)) return BQ_ERR_INVALID_ARG;
   // |a * b| <= 128 * 8 (4 bits) or 128 * 2 (2 bits): K <= 2**24 / that keeps sums exact
   const int64_t max_k = bits == 4 ? 16384 : MAX_K;
   bq_status st = check_gemm(A, Bp, M, N, K, row_scale, col_scale, C, max_k);
   if (st != BQ_OK) return st;
-  GemmArgs g{A, Bp, ACT_I8, bits, layout, M, N, K, row_scale, col_scale, EPI_I32, C};
+  GemmArgs g{A, Bp, ACT_I8, bits, layout, M, N, K, row_scale, col_scale, EPI_I32, C, activation};
   return run_gemm(g, stream);
 }
 
 bq_status bq_gemm_i8xi4(const int8_t* A, const uint8_t* Bp, int layout, int64_t M, int64_t N, int64_t K,
                         const uint16_t* row_scale, const uint16_t* col_scale, void* C, void* stream) {
-  return gemm_sub_byte(A, Bp, layout, 4, M, N, K, row_scale, col_scale, C, stream);
+  return gemm_sub_byte(A, Bp, layout, 4, M, N, K, row_scale, col_scale, BQ_ACT_NONE, C, stream);
+}
+
+bq_status bq_gemm_i8xi4_act(const int8_t* A, const uint8_t* Bp, int layout, int64_t M, int64_t N, int64_t K,
+                            const uint16_t* row_scale, const uint16_t* col_scale, int activation, void* C,
+                            void* stream) {
+  return gemm_sub_byte(A, Bp, layout, 4, M, N, K, row_scale, col_scale, activation, C, stream);
 }
 
 bq_status bq_gemm_i8xi2(const int8_t* A, const uint8_t* Bp, int layout, int64_t M, int64_t N, int64_t K,
                         const uint16_t* row_scale, const uint16_t* col_scale, void* C, void* stream) {
-  return gemm_sub_byte(A, Bp, layout, 2, M, N, K, row_scale, col_scale, C, stream);
+  return gemm_sub_byte(A, Bp, layout, 2, M, N, K, row_scale, col_scale, BQ_ACT_NONE, C, stream);
+}
+
+bq_status bq_gemm_i8xi2_act(const int8_t* A, const uint8_t* Bp, int layout, int64_t M, int64_t N, int64_t K,
+                            const uint16_t* row_scale, const uint16_t* col_scale, int activation, void* C,
+                            void* stream) {
+  return gemm_sub_byte(A, Bp, layout, 2, M, N, K, row_scale, col_scale, activation, C, stream);
 }
 
 bq_status bq_gemm_f16xi4(const uint16_t* X, const uint8_t* Wp, int layout, int64_t M, int64_t N, int64_t K,
                          const uint16_t* col_scale, uint16_t* Y, void* stream) {
+  return bq_gemm_f16xi4_act(X, Wp, layout, M, N, K, col_scale, BQ_ACT_NONE, Y, stream);
+}
+
+bq_status bq_gemm_f16xi4_act(const uint16_t* X, const uint8_t* Wp, int layout, int64_t M, int64_t N, int64_t K,
+                             const uint16_t* col_scale, int activation, uint16_t* Y, void* stream) {
   if (!valid_layout(layout)) return BQ_ERR_INVALID_ARG;
   if (M > 0 && N > 0 && !col_scale) return BQ_ERR_INVALID_ARG;
+  if (!valid_activation(activation, col_scale)) return BQ_ERR_INVALID_ARG;
   bq_status st = check_gemm(X, Wp, M, N, K, nullptr, col_scale, Y, MAX_K);
   if (st != BQ_OK) return st;
-  GemmArgs g{X, Wp, ACT_F16, 4, layout, M, N, K, nullptr, col_scale, EPI_F16_COL, Y};
+  GemmArgs g{X, Wp, ACT_F16, 4, layout, M, N, K, nullptr, col_scale, EPI_F16_COL, Y, activation};
   return run_gemm(g, stream);
 }
 

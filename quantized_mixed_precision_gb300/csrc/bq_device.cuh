@@ -128,6 +128,15 @@ __device__ __forceinline__ uint32_t plain_to_inter_i2(uint32_t w) {
   return even | (odd << 16);
 }
 
+// Activation of the fused epilogue (a bq_activation) on the fp32 dequantised
+// value, before its rounding to fp16.  GELU uses the erf form v * Phi(v),
+// written with erfc so that negative v loses nothing to cancellation.
+__device__ __forceinline__ float apply_act(float v, int actfn) {
+  if (actfn == BQ_ACT_RELU) return fmaxf(v, 0.0f);
+  if (actfn == BQ_ACT_GELU) return 0.5f * v * erfcf(-v * 0.70710678118654752f);
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory mbarriers
 // ---------------------------------------------------------------------------

@@ -39,7 +39,12 @@ struct GemmArgs {
   const uint16_t* col_scale;  // fp16 (N) or null
   int epi;                // EpiKind
   void* c;                // int32 or fp16 (M, N)
+  int actfn = BQ_ACT_NONE;  // bq_activation applied before the fp16 rounding
 };
+
+// The epilogue argument the GEMM kernels take: the EpiKind in bits 0-3 and
+// the bq_activation above them (each kernel splits it on entry).
+inline int epi_arg(const GemmArgs& g) { return g.epi | (g.actfn << 4); }
 
 // Raise a kernel's dynamic shared-memory limit once per (device, kernel), so
 // that later launches make no attribute call (e.g. inside a stream capture).

@@ -9,6 +9,7 @@
 // as one 16-byte vector each.
 #include <cuda_fp16.h>
 
+#include "bq_device.cuh"
 #include "bq_internal.h"
 
 namespace bq {
@@ -23,6 +24,8 @@ __global__ void __launch_bounds__(256) gemm_dp4a_kernel(const int8_t* __restrict
                                                         int M, int N, int K, const __half* __restrict__ row_scale,
                                                         const __half* __restrict__ col_scale, int epi,
                                                         void* __restrict__ out) {
+  const int actfn = epi >> 4;
+  epi &= 15;
   __shared__ __align__(16) int As[KW][LDS];
   __shared__ __align__(16) int Bs[KW][LDS];
   const int tid = threadIdx.x;
@@ -77,6 +80,7 @@ __global__ void __launch_bounds__(256) gemm_dp4a_kernel(const int8_t* __restrict
       } else {
         float v = __fmul_rn(__int2float_rn(acc[i][j]), __half2float(col_scale[n]));
         if (epi == EPI_F16_ROWCOL) v = __fmul_rn(v, __half2float(row_scale[m]));
+        v = apply_act(v, actfn);
         static_cast<__half*>(out)[o] = __float2half_rn(v);
       }
     }
@@ -90,7 +94,7 @@ cudaError_t launch_gemm_dp4a(const GemmArgs& g, cudaStream_t stream) {
   gemm_dp4a_kernel<<<grid, 256, 0, stream>>>(static_cast<const int8_t*>(g.a), static_cast<const int8_t*>(g.b),
                                               (int)g.M, (int)g.N, (int)g.K,
                                               reinterpret_cast<const __half*>(g.row_scale),
-                                              reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c);
+                                              reinterpret_cast<const __half*>(g.col_scale), epi_arg(g), g.c);
   return cudaGetLastError();
 }
 

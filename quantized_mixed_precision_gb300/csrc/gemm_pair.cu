@@ -120,13 +120,17 @@ struct PairCfg {
   static_assert(CONSUMER_WARPS * STG_BYTES <= OFF_BAR, "epilogue staging fits in the pipeline buffers");
 };
 
-template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16>
+// ACTV: the fp16 epilogue applies the activation in bits 4.. of `epi` (a
+// separate instantiation, so the kernel without one carries no trace of it).
+template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool ACTV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST, AF16>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, int M, int N, int K,
                      const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
                      uint64_t timeout_ns, int* status) {
   using C = PairCfg<BBITS, BN, ST, RST, AF16>;
+  const int actfn = epi >> 4;
+  epi &= 15;
   extern __shared__ uint8_t smem_raw[];
   // same offset in both CTAs: the pair MMA addresses the peer's tile by this CTA's offsets
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -387,6 +391,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
               x0 = __fmul_rn(x0, rsc);
               x1 = __fmul_rn(x1, rsc);
             }
+            if constexpr (ACTV) {
+              x0 = apply_act(x0, actfn);
+              x1 = apply_act(x1, actfn);
+            }
             const __half2 h2 = __halves2half2(__float2half_rn(x0), __float2half_rn(x1));
             hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
           }
@@ -421,7 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16>
+template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool ACTV>
 cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   using C = PairCfg<BBITS, BN, ST, RST, AF16>;
   int* status = nullptr;
@@ -442,21 +450,28 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   else
     e = make_map(&mc, g.c, 2, (uint64_t)g.N, (uint64_t)g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, AF16>;
+  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, AF16, ACTV>;
   e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(2 * ((g.M + 2 * PM - 1) / (2 * PM))), (unsigned)((g.N + BN - 1) / BN));
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(ma, mb, mc, (int)g.M, (int)g.N, (int)g.K,
                                               reinterpret_cast<const __half*>(g.row_scale),
-                                              reinterpret_cast<const __half*>(g.col_scale), g.epi,
+                                              reinterpret_cast<const __half*>(g.col_scale), epi_arg(g),
                                               (uint64_t)wait_timeout_ns(), status);
   return cudaGetLastError();
 }
 
+template <int BBITS, int BN, int ST, int RST, bool AF16, bool ACTV>
+cudaError_t launch_pair_act(const GemmArgs& g, cudaStream_t stream) {
+  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN)
+    return launch_pair_t<BBITS, BN, false, ST, RST, AF16, ACTV>(g, stream);
+  return launch_pair_t<BBITS, BN, true, ST, RST, AF16, ACTV>(g, stream);
+}
+
 template <int BBITS, int BN, int ST, int RST, bool AF16 = false>
 cudaError_t launch_pair_layout(const GemmArgs& g, cudaStream_t stream) {
-  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN) return launch_pair_t<BBITS, BN, false, ST, RST, AF16>(g, stream);
-  return launch_pair_t<BBITS, BN, true, ST, RST, AF16>(g, stream);
+  if (g.actfn != BQ_ACT_NONE) return launch_pair_act<BBITS, BN, ST, RST, AF16, true>(g, stream);
+  return launch_pair_act<BBITS, BN, ST, RST, AF16, false>(g, stream);
 }
 
 cudaError_t launch_pair_f16(const GemmArgs& g, int bn, cudaStream_t stream) {

@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
                      int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale,
                      int epi, void* __restrict__ out, uint64_t timeout_ns, int* status) {
   using C = SwapCfg<BBITS, MN>;
+  const int actfn = epi >> 4;
+  epi &= 15;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);   // TMEM weight stage written
@@ -278,6 +280,7 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
             } else {
               float y = __fmul_rn(acc, cs);
               if (epi == EPI_F16_ROWCOL) y = __fmul_rn(y, __half2float(row_scale[m]));
+              y = apply_act(y, actfn);
               static_cast<__half*>(out)[o] = __float2half_rn(y);
             }
           }
@@ -322,7 +325,7 @@ cudaError_t launch_swap_t(const GemmArgs& g, cudaStream_t stream) {
   const int M = (int)g.M, N = (int)g.N, K = (int)g.K;
   const __half* rsc = reinterpret_cast<const __half*>(g.row_scale);
   const __half* csc = reinterpret_cast<const __half*>(g.col_scale);
-  const int epi = g.epi;
+  const int epi = epi_arg(g);
   void* out = g.c;
   const uint64_t to = (uint64_t)wait_timeout_ns();
   e = cudaLaunchKernelEx(&cfg, kern, mw, mx, M, N, K, rsc, csc, epi, out, to, status);

@@ -194,6 +194,8 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
                    int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
                    void* __restrict__ out, uint64_t timeout_ns, int* status) {
   using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>;
+  const int actfn = epi >> 4;
+  epi &= 15;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);   // MMA stage ready
@@ -443,6 +445,8 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
                 x0 = __fmul_rn(x0, rsc);
                 x1 = __fmul_rn(x1, rsc);
               }
+              x0 = apply_act(x0, actfn);
+              x1 = apply_act(x1, actfn);
               const __half2 h2 = __halves2half2(__float2half_rn(x0), __float2half_rn(x1));
               hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
             }
@@ -542,6 +546,8 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
                   x0 = __fmul_rn(x0, rsc);
                   x1 = __fmul_rn(x1, rsc);
                 }
+                x0 = apply_act(x0, actfn);
+                x1 = apply_act(x1, actfn);
                 const __half2 h2 = __halves2half2(__float2half_rn(x0), __float2half_rn(x1));
                 hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
               }
@@ -604,7 +610,7 @@ cudaError_t launch_t(const GemmArgs& g, int split, cudaStream_t stream) {
   const int M = (int)g.M, N = (int)g.N, K = (int)g.K;
   const __half* rsc = reinterpret_cast<const __half*>(g.row_scale);
   const __half* csc = reinterpret_cast<const __half*>(g.col_scale);
-  const int epi = g.epi;
+  const int epi = epi_arg(g);
   void* out = g.c;
   const uint64_t to = (uint64_t)wait_timeout_ns();
   e = cudaLaunchKernelEx(&cfg, kern, ma, mb, M, N, K, rsc, csc, epi, out, to, status);

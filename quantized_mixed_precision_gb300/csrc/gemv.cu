@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
                                                                       const __half* __restrict__ col_scale, int epi,
                                                                       void* __restrict__ out) {
   using C = GemvCfg<BBITS>;
+  const int actfn = epi >> 4;
+  epi &= 15;
   __shared__ float red[GEMV_WARPS][NB][4][32];
   extern __shared__ __align__(16) uint8_t xs[];       // M staged activation rows, then 16 zero bytes
   const int rs = gemv_row_stride<BBITS, ACT>(K);
@@ -223,6 +225,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 5) gemv_mma_kernel(const void
       } else {
         float v = __fmul_rn(acc, __half2float(col_scale[n]));
         if (epi == EPI_F16_ROWCOL) v = __fmul_rn(v, __half2float(row_scale[m]));
+        v = apply_act(v, actfn);
         static_cast<__half*>(out)[o] = __float2half_rn(v);
       }
     }
@@ -293,6 +296,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
                                                                     void* __restrict__ out, uint64_t timeout_ns,
                                                                     int* status) {
   using C = GemvCfg<BBITS>;
+  const int actfn = epi >> 4;
+  epi &= 15;
   __shared__ float red[GEMV_WARPS][NB][4][32];
   __shared__ __align__(8) uint64_t wbar[GEMV_WARPS];
   __shared__ __align__(8) uint64_t xbar[GEMV_WARPS];
@@ -438,6 +443,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
       } else {
         float v = __fmul_rn(acc, __half2float(col_scale[n]));
         if (epi == EPI_F16_ROWCOL) v = __fmul_rn(v, __half2float(row_scale[m]));
+        v = apply_act(v, actfn);
         static_cast<__half*>(out)[o] = __float2half_rn(v);
       }
     }
@@ -470,7 +476,7 @@ cudaError_t launch_bulk(const GemmArgs& g, cudaStream_t stream) {
   int M = (int)g.M, N = (int)g.N, K = (int)g.K;
   const __half* rsc = reinterpret_cast<const __half*>(g.row_scale);
   const __half* csc = reinterpret_cast<const __half*>(g.col_scale);
-  int epi = g.epi;
+  int epi = epi_arg(g);
   void* c = g.c;
   uint64_t to = (uint64_t)wait_timeout_ns();
   e = cudaLaunchKernelEx(&cfg, kern, a, b, M, N, K, rsc, csc, epi, c, to, status);
@@ -488,7 +494,7 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
   }
   kern<<<(unsigned)(g.N / 16), GEMV_WARPS * 32, smem, stream>>>(
       g.a, static_cast<const uint8_t*>(g.b), (int)g.M, (int)g.N, (int)g.K,
-      reinterpret_cast<const __half*>(g.row_scale), reinterpret_cast<const __half*>(g.col_scale), g.epi, g.c);
+      reinterpret_cast<const __half*>(g.row_scale), reinterpret_cast<const __half*>(g.col_scale), epi_arg(g), g.c);
   return cudaGetLastError();
 }
 

@@ -23,6 +23,7 @@ def lib():
 EXPECTED = sorted([
     "bq_status_string", "bq_quantize_sym", "bq_packed_size", "bq_pack_weights", "bq_gemm_i8xi8",
     "bq_gemm_i8xi4", "bq_gemm_i8xi2", "bq_gemm_f16xi4", "bq_device_status", "bq_set_wait_timeout_ns",
+    "bq_gemm_i8xi8_act", "bq_gemm_i8xi4_act", "bq_gemm_i8xi2_act", "bq_gemm_f16xi4_act",
 ])
 
 FAKE = ctypes.c_void_p(0x10000)     # aligned, never dereferenced
@@ -115,6 +116,38 @@ def test_i8xi8_and_f16xi4_validation(lib):
     assert g(FAKE, FAKE, 1, 4, 64, 64, None, FAKE, None) == bq.BQ_ERR_INVALID_ARG   # scale required
     assert g(FAKE, FAKE, 1, 4, 64, 64, FAKE, FAKE_ODD, None) == bq.BQ_ERR_ALIGNMENT
     assert g(FAKE, FAKE, 0, 0, 64, 64, None, None, None) == bq.BQ_OK
+
+
+@pytest.mark.parametrize("name", ["bq_gemm_i8xi4_act", "bq_gemm_i8xi2_act"])
+def test_packed_gemm_act_validation(lib, name):
+    f = getattr(lib, name)
+    ok = dict(A=FAKE, B=FAKE, L=1, M=32, N=64, K=64, rs=None, cs=FAKE, act=bq.ACT_GELU, C=FAKE)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["A"], a["B"], a["L"], a["M"], a["N"], a["K"], a["rs"], a["cs"], a["act"], a["C"], None)
+
+    assert call(act=3) == bq.BQ_ERR_INVALID_ARG
+    assert call(act=-1) == bq.BQ_ERR_INVALID_ARG
+    assert call(cs=None) == bq.BQ_ERR_INVALID_ARG               # an activation needs the fp16 output
+    assert call(cs=None, act=bq.ACT_RELU, M=0) == bq.BQ_ERR_INVALID_ARG
+    assert call(cs=None, act=bq.ACT_NONE, M=0) == bq.BQ_OK      # int32 output without activation
+    assert call(L=5) == bq.BQ_ERR_INVALID_ARG
+    assert call(K=96) == bq.BQ_ERR_UNSUPPORTED
+    assert call(A=FAKE_ODD) == bq.BQ_ERR_ALIGNMENT
+    assert call(M=0) == bq.BQ_OK
+
+
+def test_i8xi8_and_f16xi4_act_validation(lib):
+    f = lib.bq_gemm_i8xi8_act
+    assert f(FAKE, FAKE, 4, 64, 64, None, FAKE, 9, FAKE, None) == bq.BQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 4, 64, 64, None, None, bq.ACT_RELU, FAKE, None) == bq.BQ_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 0, 64, 64, None, FAKE, bq.ACT_GELU, FAKE, None) == bq.BQ_OK
+    g = lib.bq_gemm_f16xi4_act
+    assert g(FAKE, FAKE, 1, 4, 64, 64, FAKE, 7, FAKE, None) == bq.BQ_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, 1, 4, 64, 64, None, bq.ACT_GELU, FAKE, None) == bq.BQ_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, 1, 4, 64, 64, FAKE, bq.ACT_RELU, FAKE_ODD, None) == bq.BQ_ERR_ALIGNMENT
+    assert g(FAKE, FAKE, 1, 0, 64, 64, FAKE, bq.ACT_GELU, FAKE, None) == bq.BQ_OK
 
 
 def test_device_status_null(lib):

@@ -38,7 +38,13 @@ def host(t):
     return t.cpu().numpy()
 
 
-def assert_f16_close(y, y_ref, scale_ij, what=""):
+def assert_f16_close(y, y_ref, scale_ij, what="", f16_ulps=0):
+    """f16_ulps > 0 also admits that many units in the last place of the
+    fp16 reference: for outputs whose last step is evaluated in different
+    precisions on the two sides (an fp32 activation against the oracle's
+    float64 one), the single rounding to fp16 may land one step apart, and
+    in the fp16 subnormal range one step exceeds the relative tolerance."""
+    ulp = np.spacing(np.abs(y_ref.astype(np.float16))).astype(np.float64)
     y = y.astype(np.float64)
     y_ref = y_ref.astype(np.float64)
     inf_ref = ~np.isfinite(y_ref)
@@ -46,6 +52,8 @@ def assert_f16_close(y, y_ref, scale_ij, what=""):
     assert (y[inf_ref] == y_ref[inf_ref]).all(), f"{what}: inf sign differs"
     fin = ~inf_ref
     tol = np.maximum(1e-3 * np.abs(y_ref), 1e-3 * np.broadcast_to(scale_ij, y_ref.shape).astype(np.float64))
+    if f16_ulps:
+        tol = np.maximum(tol, f16_ulps * ulp)
     err = np.abs(y - y_ref)
     bad = fin & (err > tol)
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; "
@@ -223,6 +231,54 @@ def test_f16xi4_parity(M, N, K, layout):
     s = W.uniform_f16(rng, (N,), 0.008, 0.016)
     y = host(bq.bq_gemm_f16xi4(dev(X), dev(O.pack(q, 4, layout)), dev(s), layout))
     assert_f16_close(y, O.gemm_f16xq(X, q, s), s[None, :].astype(np.float64), "f16xi4")
+
+
+# ---------------------------------------------------------------------------
+# fused activation epilogue (ReLU, GELU) on every path: skinny kernels, the
+# single-CTA tensor-core kernel (K split over a cluster), CTA pairs, the
+# small-M fp16 kernel
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("act", ["relu", "gelu"])
+@pytest.mark.parametrize("bits,M,N,K", [(8, 1, 64, 256), (8, 40, 192, 256), (8, 600, 8192, 256),
+                                        (4, 1, 128, 512), (4, 40, 320, 512), (4, 600, 8192, 256),
+                                        (2, 3, 128, 512), (2, 200, 256, 512), (2, 600, 8192, 256)])
+def test_int_gemm_activation(act, bits, M, N, K):
+    rng = np.random.default_rng(bits * 7 + M + N + K)
+    A = W.int8_uniform(rng, (M, K))
+    Bq = _codes(rng, bits, (N, K))
+    sw = W.uniform_f16(rng, (N,), 1e-3, 1e-2)
+    sx = W.uniform_f16(rng, (M,), 1e-3, 1e-1)
+    y_ref = O.dequant(O.gemm_int(A, Bq), sw, sx, act=act)
+    rs, cs = dev(sx), dev(sw)
+    if bits == 8:
+        y = bq.bq_gemm_i8xi8_act(dev(A), dev(Bq), act, row_scale=rs, col_scale=cs)
+    else:
+        fn = bq.bq_gemm_i8xi4_act if bits == 4 else bq.bq_gemm_i8xi2_act
+        y = fn(dev(A), dev(O.pack(Bq, bits, "interleaved")), act, "interleaved", row_scale=rs, col_scale=cs)
+    assert_f16_close(host(y), y_ref, (sx[:, None].astype(np.float64) * sw[None, :]), f"{act} bits {bits}",
+                     f16_ulps=1 if act == "gelu" else 0)
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu"])
+@pytest.mark.parametrize("M,N,K", [(1, 320, 512), (5, 128, 832), (40, 4160, 320), (512, 8192, 256)])
+def test_f16xi4_activation(act, M, N, K):
+    rng = np.random.default_rng(M + N + K + (0 if act == "relu" else 1))
+    X = W.normal_f16(rng, (M, K), 1.0)
+    q = W.int4_uniform(rng, (N, K))
+    s = W.uniform_f16(rng, (N,), 0.008, 0.016)
+    y = host(bq.bq_gemm_f16xi4_act(dev(X), dev(O.pack(q, 4, "interleaved")), dev(s), act))
+    assert_f16_close(y, O.gemm_f16xq(X, q, s, act=act), s[None, :].astype(np.float64), f"f16xi4 {act}",
+                     f16_ulps=1 if act == "gelu" else 0)
+
+
+def test_activation_none_matches_plain_call():
+    rng = np.random.default_rng(11)
+    A = W.int8_uniform(rng, (64, 256))
+    Bp = dev(O.pack(W.int4_uniform(rng, (192, 256)), 4, "interleaved"))
+    sw = dev(W.uniform_f16(rng, (192,), 1e-3, 1e-2))
+    a = host(bq.bq_gemm_i8xi4(dev(A), Bp, "interleaved", col_scale=sw))
+    b = host(bq.bq_gemm_i8xi4_act(dev(A), Bp, "none", "interleaved", col_scale=sw))
+    assert (a.view(np.uint16) == b.view(np.uint16)).all()
 
 
 @pytest.mark.parametrize("M,N,K", [(2, 320, 2048), (8, 192, 512), (3, 64, 1344), (5, 128, 832)])

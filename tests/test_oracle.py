@@ -328,3 +328,66 @@ def test_roofline_helper_printed_numbers():
     assert roofline.matmul_min_bytes(m, k, n, bits, bits, bits) == int(g["membw_bytes"])
     # packed 4-bit weights count half a byte per element
     assert roofline.matmul_min_bytes(4096, 4096, 4096, 8, 4, 16) == (16 + 8 + 32) * 2 ** 20
+
+
+# ---------------------------------------------------------------------------
+# fused activation (reading Q15): pinned to tabulated values of the standard
+# normal distribution function and to identities, not to the formula itself
+# ---------------------------------------------------------------------------
+def test_gelu_tabulated_values():
+    # Phi(1) = 0.8413447460685429 and Phi(3) = 0.9986501019683699 (standard
+    # normal table), so GELU(1) = Phi(1) and GELU(-3) = -3 * (1 - Phi(3)).
+    g = O.activation(np.array([1.0, -3.0, 0.0]), "gelu")
+    assert g[0] == pytest.approx(0.8413447460685429, rel=1e-15)
+    assert g[1] == pytest.approx(-3.0 * (1.0 - 0.9986501019683699), rel=1e-12)
+    assert g[2] == 0.0
+
+
+def test_gelu_odd_part_and_limits():
+    # Phi(v) + Phi(-v) = 1  =>  GELU(v) - GELU(-v) = v  (a sign or argument slip breaks it)
+    v = np.linspace(-6.0, 6.0, 97)
+    g = O.activation(v, "gelu")
+    gm = O.activation(-v, "gelu")
+    assert np.allclose(g - gm, v, rtol=0, atol=1e-14)
+    # far tails: identity for large v, vanishing (and negative) for very negative v
+    assert O.activation(np.array([40.0]), "gelu")[0] == 40.0
+    tail = O.activation(np.array([-12.0]), "gelu")[0]
+    assert -1e-30 < tail < 0.0
+    # monotone from its minimum near v = -0.75 on
+    w = np.linspace(-0.7, 5.0, 200)
+    assert (np.diff(O.activation(w, "gelu")) > 0).all()
+
+
+def test_relu_and_none():
+    v = np.array([-2.5, -0.0, 0.0, 1e-8, 3.0])
+    assert O.activation(v, "relu").tolist() == [0.0, 0.0, 0.0, 1e-8, 3.0]
+    assert O.activation(v, "none").tolist() == v.tolist()
+    with pytest.raises(ValueError):
+        O.activation(v, "tanh")
+
+
+def test_dequant_relu_commutes_with_rounding():
+    # RNE to fp16 is monotone and maps 0 to 0, so ReLU before the rounding
+    # equals clamping the rounded value; a dropped activation, or min taken
+    # for max, fails this.
+    rng = np.random.default_rng(5)
+    c = rng.integers(-40000, 40000, size=(7, 64)).astype(np.int32)
+    sw = W.uniform_f16(rng, (64,), 1e-3, 1e-2)
+    sx = W.uniform_f16(rng, (7,), 1e-3, 1e-1)
+    base = O.dequant(c, sw, sx).astype(np.float64)
+    assert (O.dequant(c, sw, sx, act="relu").astype(np.float64) == np.maximum(base, 0.0)).all()
+    assert (O.dequant(c, sw, sx, act="none") == O.dequant(c, sw, sx)).all()
+
+
+def test_f16xq_gelu_positive_scale_preserves_sign_of_dequant():
+    rng = np.random.default_rng(6)
+    x = W.normal_f16(rng, (3, 128), 1.0)
+    q = W.int4_uniform(rng, (32, 128))
+    s = W.uniform_f16(rng, (32,), 0.008, 0.016)
+    y = O.gemm_f16xq(x, q, s).astype(np.float64)
+    yg = O.gemm_f16xq(x, q, s, act="gelu").astype(np.float64)
+    # GELU(v) has the sign of v, |GELU(v)| <= |v|, and GELU(v) >= v / 2 for v >= 0
+    assert (np.sign(yg) * np.sign(y) >= 0).all()
+    assert (np.abs(yg) <= np.abs(y) + 1e-3).all()
+    pos = y > 0.05
+    assert (yg[pos] >= 0.5 * y[pos] - 1e-3).all()
