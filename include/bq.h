@@ -206,6 +206,42 @@ bq_status bq_gemm_f16xi4_act(const uint16_t* X, const uint8_t* Wp, int layout, i
                              void* stream);
 
 /*
+ * Batched GEMMs with broadcast operands.  [BMINF 實現代碼分析2: igemm takes
+ * (batch, rows, k) operands, and an operand whose batch is 1 is shared by
+ * every item (stride 0); the fused QKV projection multiplies one block of
+ * activations by the three stacked weight matrices, w_project_qkv (3, N, K)]
+ *
+ *   For every b in [0, batch):
+ *     C + b*stride_c = the unbatched call on A + b*stride_a, B + b*stride_b,
+ *                      row_scale + b*stride_rs, col_scale + b*stride_cs
+ *   with that call's semantics, limits, dispatch and activation.  Strides
+ *   count elements of each array (bytes for packed weights); a stride of 0
+ *   broadcasts the operand.  stride_c must be at least M * N when batch > 1
+ *   (outputs never overlap).  Every item's pointers must be 16-byte aligned,
+ *   i.e. aligned bases and strides whose byte size is a multiple of 16.
+ *   All items are validated before the first launch; they are launched in
+ *   order on `stream`, one after another.
+ *   Errors: as the unbatched call; INVALID_ARG also for batch < 0, a
+ *   negative stride or overlapping outputs.
+ */
+bq_status bq_gemm_i8xi8_batched(const int8_t* A, int64_t stride_a, const int8_t* B, int64_t stride_b,
+                                int64_t batch, int64_t M, int64_t N, int64_t K,
+                                const uint16_t* row_scale, int64_t stride_rs, const uint16_t* col_scale,
+                                int64_t stride_cs, int activation, void* C, int64_t stride_c, void* stream);
+bq_status bq_gemm_i8xi4_batched(const int8_t* A, int64_t stride_a, const uint8_t* Bp, int64_t stride_b,
+                                int layout, int64_t batch, int64_t M, int64_t N, int64_t K,
+                                const uint16_t* row_scale, int64_t stride_rs, const uint16_t* col_scale,
+                                int64_t stride_cs, int activation, void* C, int64_t stride_c, void* stream);
+bq_status bq_gemm_i8xi2_batched(const int8_t* A, int64_t stride_a, const uint8_t* Bp, int64_t stride_b,
+                                int layout, int64_t batch, int64_t M, int64_t N, int64_t K,
+                                const uint16_t* row_scale, int64_t stride_rs, const uint16_t* col_scale,
+                                int64_t stride_cs, int activation, void* C, int64_t stride_c, void* stream);
+bq_status bq_gemm_f16xi4_batched(const uint16_t* X, int64_t stride_x, const uint8_t* Wp, int64_t stride_w,
+                                 int layout, int64_t batch, int64_t M, int64_t N, int64_t K,
+                                 const uint16_t* col_scale, int64_t stride_cs, int activation, uint16_t* Y,
+                                 int64_t stride_y, void* stream);
+
+/*
  * Device-side wait status.  Every wait inside the tensor-core kernels and the
  * skinny kernel (on a shared-memory mbarrier) is bounded in time.  A wait that gives up records
  * BQ_ERR_TIMEOUT in a device status word, abandons the tile, waits (again

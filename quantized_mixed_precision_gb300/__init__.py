@@ -46,6 +46,14 @@ _SIGNATURES = {
                                          _vp, _vp]),
     "bq_gemm_f16xi4_act": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, ctypes.c_int, _vp,
                                           _vp]),
+    "bq_gemm_i8xi8_batched": (ctypes.c_int, [_vp, _c_i64, _vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64, _vp, _c_i64,
+                                             _vp, _c_i64, ctypes.c_int, _vp, _c_i64, _vp]),
+    "bq_gemm_i8xi4_batched": (ctypes.c_int, [_vp, _c_i64, _vp, _c_i64, ctypes.c_int, _c_i64, _c_i64, _c_i64, _c_i64,
+                                             _vp, _c_i64, _vp, _c_i64, ctypes.c_int, _vp, _c_i64, _vp]),
+    "bq_gemm_i8xi2_batched": (ctypes.c_int, [_vp, _c_i64, _vp, _c_i64, ctypes.c_int, _c_i64, _c_i64, _c_i64, _c_i64,
+                                             _vp, _c_i64, _vp, _c_i64, ctypes.c_int, _vp, _c_i64, _vp]),
+    "bq_gemm_f16xi4_batched": (ctypes.c_int, [_vp, _c_i64, _vp, _c_i64, ctypes.c_int, _c_i64, _c_i64, _c_i64, _c_i64,
+                                              _vp, _c_i64, ctypes.c_int, _vp, _c_i64, _vp]),
     "bq_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "bq_set_wait_timeout_ns": (_c_i64, [_c_i64]),
 }
@@ -293,6 +301,82 @@ def bq_gemm_f16xi4_act(X, Wp, col_scale, activation, layout=LAYOUT_INTERLEAVED, 
                                   _activation(activation), _ptr(out), _stream(stream))
     _check(st, "bq_gemm_f16xi4_act")
     return out
+
+
+def _batch_stride(t, batch, name):
+    """Element stride between the batch items of an operand whose first
+    dimension is its batch; a batch of 1 is shared by every item (stride 0)."""
+    lead = t.shape[0]
+    if lead not in (1, batch):
+        raise ValueError(f"{name}: batch dimension {lead} is neither 1 nor {batch}")
+    return 0 if lead == 1 else t[0].numel()
+
+
+def _scale_stride(t, batch, name):
+    """Scales are (n,) -- shared by every item -- or (batch or 1, n)."""
+    if t is None or t.dim() == 1:
+        return 0
+    return _batch_stride(t, batch, name)
+
+
+def _batched(fn_name, A, Bw, bits, layout, row_scale, col_scale, activation, out, stream, act_type):
+    torch = _torch()
+    _need(A, act_type, "A", 3)
+    _need(Bw, torch.int8 if bits == 8 else torch.uint8, "B", 3)
+    batch = max(A.shape[0], Bw.shape[0])
+    M, K = A.shape[1], A.shape[2]
+    N = Bw.shape[1]
+    if Bw.shape[2] * 8 != K * bits:
+        raise ValueError("weight width does not match K")
+    for t, nm in ((row_scale, "row_scale"), (col_scale, "col_scale")):
+        if t is not None:
+            _need(t, torch.float16, nm)
+    scaled = col_scale is not None
+    dtype = torch.float16 if scaled else torch.int32
+    if out is None:
+        out = torch.empty((batch, M, N), dtype=dtype, device=A.device)
+    _need(out, dtype, "out", 3)
+    sa = _batch_stride(A, batch, "A")
+    sb = _batch_stride(Bw, batch, "B")
+    srs = _scale_stride(row_scale, batch, "row_scale")
+    scs = _scale_stride(col_scale, batch, "col_scale")
+    sc = M * N
+    f = getattr(lib(), fn_name)
+    if fn_name == "bq_gemm_f16xi4_batched":
+        st = f(_ptr(A), sa, _ptr(Bw), sb, _layout(layout), batch, M, N, K, _ptr(col_scale), scs,
+               _activation(activation), _ptr(out), sc, _stream(stream))
+    elif fn_name == "bq_gemm_i8xi8_batched":
+        st = f(_ptr(A), sa, _ptr(Bw), sb, batch, M, N, K, _ptr(row_scale), srs, _ptr(col_scale), scs,
+               _activation(activation), _ptr(out), sc, _stream(stream))
+    else:
+        st = f(_ptr(A), sa, _ptr(Bw), sb, _layout(layout), batch, M, N, K, _ptr(row_scale), srs, _ptr(col_scale),
+               scs, _activation(activation), _ptr(out), sc, _stream(stream))
+    _check(st, fn_name)
+    return out
+
+
+def bq_gemm_i8xi8_batched(A, B, row_scale=None, col_scale=None, activation="none", out=None, stream=None):
+    """A (Ba, M, K) int8, B (Bb, N, K) int8 with Ba, Bb in {1, batch} (1 = shared by every item);
+    scales (batch or 1, M / N) or (M,) / (N,); out (batch, M, N)."""
+    return _batched("bq_gemm_i8xi8_batched", A, B, 8, LAYOUT_PLAIN, row_scale, col_scale, activation, out, stream,
+                    _torch().int8)
+
+
+def bq_gemm_i8xi4_batched(A, Bp, layout=LAYOUT_INTERLEAVED, row_scale=None, col_scale=None, activation="none",
+                          out=None, stream=None):
+    return _batched("bq_gemm_i8xi4_batched", A, Bp, 4, layout, row_scale, col_scale, activation, out, stream,
+                    _torch().int8)
+
+
+def bq_gemm_i8xi2_batched(A, Bp, layout=LAYOUT_INTERLEAVED, row_scale=None, col_scale=None, activation="none",
+                          out=None, stream=None):
+    return _batched("bq_gemm_i8xi2_batched", A, Bp, 2, layout, row_scale, col_scale, activation, out, stream,
+                    _torch().int8)
+
+
+def bq_gemm_f16xi4_batched(X, Wp, col_scale, layout=LAYOUT_INTERLEAVED, activation="none", out=None, stream=None):
+    return _batched("bq_gemm_f16xi4_batched", X, Wp, 4, layout, None, col_scale, activation, out, stream,
+                    _torch().float16)
 
 
 def bq_device_status(reset=True) -> int:

@@ -14,6 +14,15 @@ std::atomic<int64_t> g_wait_timeout_ns{2000000000LL};
 constexpr int64_t MAX_K = 65536;
 constexpr int64_t MAX_DIM = 1LL << 24;
 constexpr int64_t SKINNY_M = 16;
+constexpr int64_t MAX_STRIDE = 1LL << 46;   // bytes; with MAX_BATCH, every item offset stays below 2**62
+constexpr int64_t MAX_BATCH = 1LL << 16;
+
+// A stride in elements as bytes: negative stays negative (rejected), a huge
+// one saturates above MAX_STRIDE (rejected) instead of overflowing.
+inline int64_t stride_bytes(int64_t s, int64_t elem) {
+  if (s < 0) return -1;
+  return s > MAX_STRIDE ? MAX_STRIDE + 16 : s * elem;
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -64,6 +73,38 @@ bq_status run_gemm(GemmArgs g, void* stream) {
     e = launch_gemm_tc(g, s);
   }
   return from_cuda(e);
+}
+
+// Batched calls: item b uses every pointer advanced by b times its stride
+// (in bytes here; 0 broadcasts).  Validates once for all items -- the items
+// differ from the first only by offsets that are multiples of 16 bytes --
+// then launches them in order.
+bq_status run_batched(const GemmArgs& g, int64_t batch, int64_t sa, int64_t sb, int64_t srs, int64_t scs,
+                      int64_t sc, int64_t max_k, void* stream) {
+  if (batch < 0 || sa < 0 || sb < 0 || srs < 0 || scs < 0 || sc < 0) return BQ_ERR_INVALID_ARG;
+  if (batch == 0) return BQ_OK;
+  bq_status st = check_gemm(g.a, g.b, g.M, g.N, g.K, g.row_scale, g.col_scale, g.c, max_k);
+  if (st != BQ_OK) return st;
+  if (g.M == 0 || g.N == 0) return BQ_OK;
+  if (batch > 1) {
+    const int64_t out_bytes = g.M * g.N * (g.col_scale ? 2 : 4);
+    if (sc < out_bytes) return BQ_ERR_INVALID_ARG;   // outputs would overlap
+    if ((sa | sb | srs | scs | sc) % 16 != 0) return BQ_ERR_ALIGNMENT;
+    if (sa > MAX_STRIDE || sb > MAX_STRIDE || srs > MAX_STRIDE || scs > MAX_STRIDE || sc > MAX_STRIDE ||
+        batch > MAX_BATCH)
+      return BQ_ERR_UNSUPPORTED;
+  }
+  for (int64_t b = 0; b < batch; ++b) {
+    GemmArgs gi = g;
+    gi.a = static_cast<const uint8_t*>(g.a) + b * sa;
+    gi.b = static_cast<const uint8_t*>(g.b) + b * sb;
+    if (g.row_scale) gi.row_scale = reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(g.row_scale) + b * srs);
+    if (g.col_scale) gi.col_scale = reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(g.col_scale) + b * scs);
+    gi.c = static_cast<uint8_t*>(g.c) + b * sc;
+    st = run_gemm(gi, stream);
+    if (st != BQ_OK) return st;
+  }
+  return BQ_OK;
 }
 
 }  // namespace
@@ -202,6 +243,54 @@ bq_status bq_gemm_f16xi4_act(const uint16_t* X, const uint8_t* Wp, int layout, i
   if (st != BQ_OK) return st;
   GemmArgs g{X, Wp, ACT_F16, 4, layout, M, N, K, nullptr, col_scale, EPI_F16_COL, Y, activation};
   return run_gemm(g, stream);
+}
+
+bq_status bq_gemm_i8xi8_batched(const int8_t* A, int64_t stride_a, const int8_t* B, int64_t stride_b, int64_t batch,
+                                int64_t M, int64_t N, int64_t K, const uint16_t* row_scale, int64_t stride_rs,
+                                const uint16_t* col_scale, int64_t stride_cs, int activation, void* C,
+                                int64_t stride_c, void* stream) {
+  if (!valid_activation(activation, col_scale)) return BQ_ERR_INVALID_ARG;
+  GemmArgs g{A, B, ACT_I8, 8, BQ_LAYOUT_PLAIN, M, N, K, row_scale, col_scale, EPI_I32, C, activation};
+  return run_batched(g, batch, stride_bytes(stride_a, 1), stride_bytes(stride_b, 1), stride_bytes(stride_rs, 2),
+                     stride_bytes(stride_cs, 2), stride_bytes(stride_c, col_scale ? 2 : 4), MAX_K, stream);
+}
+
+static bq_status sub_byte_batched(const int8_t* A, int64_t stride_a, const uint8_t* Bp, int64_t stride_b, int layout,
+                                  int bits, int64_t batch, int64_t M, int64_t N, int64_t K,
+                                  const uint16_t* row_scale, int64_t stride_rs, const uint16_t* col_scale,
+                                  int64_t stride_cs, int activation, void* C, int64_t stride_c, void* stream) {
+  if (!valid_layout(layout) || !valid_activation(activation, col_scale)) return BQ_ERR_INVALID_ARG;
+  const int64_t max_k = bits == 4 ? 16384 : MAX_K;
+  GemmArgs g{A, Bp, ACT_I8, bits, layout, M, N, K, row_scale, col_scale, EPI_I32, C, activation};
+  return run_batched(g, batch, stride_bytes(stride_a, 1), stride_bytes(stride_b, 1), stride_bytes(stride_rs, 2),
+                     stride_bytes(stride_cs, 2), stride_bytes(stride_c, col_scale ? 2 : 4), max_k, stream);
+}
+
+bq_status bq_gemm_i8xi4_batched(const int8_t* A, int64_t stride_a, const uint8_t* Bp, int64_t stride_b, int layout,
+                                int64_t batch, int64_t M, int64_t N, int64_t K, const uint16_t* row_scale,
+                                int64_t stride_rs, const uint16_t* col_scale, int64_t stride_cs, int activation,
+                                void* C, int64_t stride_c, void* stream) {
+  return sub_byte_batched(A, stride_a, Bp, stride_b, layout, 4, batch, M, N, K, row_scale, stride_rs, col_scale,
+                          stride_cs, activation, C, stride_c, stream);
+}
+
+bq_status bq_gemm_i8xi2_batched(const int8_t* A, int64_t stride_a, const uint8_t* Bp, int64_t stride_b, int layout,
+                                int64_t batch, int64_t M, int64_t N, int64_t K, const uint16_t* row_scale,
+                                int64_t stride_rs, const uint16_t* col_scale, int64_t stride_cs, int activation,
+                                void* C, int64_t stride_c, void* stream) {
+  return sub_byte_batched(A, stride_a, Bp, stride_b, layout, 2, batch, M, N, K, row_scale, stride_rs, col_scale,
+                          stride_cs, activation, C, stride_c, stream);
+}
+
+bq_status bq_gemm_f16xi4_batched(const uint16_t* X, int64_t stride_x, const uint8_t* Wp, int64_t stride_w, int layout,
+                                 int64_t batch, int64_t M, int64_t N, int64_t K, const uint16_t* col_scale,
+                                 int64_t stride_cs, int activation, uint16_t* Y, int64_t stride_y, void* stream) {
+  if (!valid_layout(layout)) return BQ_ERR_INVALID_ARG;
+  if (M > 0 && N > 0 && !col_scale) return BQ_ERR_INVALID_ARG;
+  if (!valid_activation(activation, col_scale)) return BQ_ERR_INVALID_ARG;
+  GemmArgs g{X, Wp, ACT_F16, 4, layout, M, N, K, nullptr, col_scale, EPI_F16_COL, Y, activation};
+  return run_batched(g, batch, stride_bytes(stride_x, 2), stride_bytes(stride_w, 1), 0, stride_bytes(stride_cs, 2),
+                     stride_bytes(stride_y, 2), MAX_K, stream);
 }
 
 bq_status bq_device_status(int* status_out, int reset) {

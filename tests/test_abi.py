@@ -24,6 +24,7 @@ EXPECTED = sorted([
     "bq_status_string", "bq_quantize_sym", "bq_packed_size", "bq_pack_weights", "bq_gemm_i8xi8",
     "bq_gemm_i8xi4", "bq_gemm_i8xi2", "bq_gemm_f16xi4", "bq_device_status", "bq_set_wait_timeout_ns",
     "bq_gemm_i8xi8_act", "bq_gemm_i8xi4_act", "bq_gemm_i8xi2_act", "bq_gemm_f16xi4_act",
+    "bq_gemm_i8xi8_batched", "bq_gemm_i8xi4_batched", "bq_gemm_i8xi2_batched", "bq_gemm_f16xi4_batched",
 ])
 
 FAKE = ctypes.c_void_p(0x10000)     # aligned, never dereferenced
@@ -148,6 +149,34 @@ def test_i8xi8_and_f16xi4_act_validation(lib):
     assert g(FAKE, FAKE, 1, 4, 64, 64, None, bq.ACT_GELU, FAKE, None) == bq.BQ_ERR_INVALID_ARG
     assert g(FAKE, FAKE, 1, 4, 64, 64, FAKE, bq.ACT_RELU, FAKE_ODD, None) == bq.BQ_ERR_ALIGNMENT
     assert g(FAKE, FAKE, 1, 0, 64, 64, FAKE, bq.ACT_GELU, FAKE, None) == bq.BQ_OK
+
+
+def test_batched_validation(lib):
+    f = lib.bq_gemm_i8xi4_batched
+    # A, sa, Bp, sb, layout, batch, M, N, K, rs, srs, cs, scs, act, C, sc, stream
+    ok = dict(A=FAKE, sa=0, B=FAKE, sb=64 * 32, L=1, batch=3, M=32, N=64, K=64, rs=None, srs=0, cs=FAKE, scs=64,
+              act=0, C=FAKE, sc=32 * 64)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["A"], a["sa"], a["B"], a["sb"], a["L"], a["batch"], a["M"], a["N"], a["K"], a["rs"], a["srs"],
+                 a["cs"], a["scs"], a["act"], a["C"], a["sc"], None)
+
+    assert call(batch=-1) == bq.BQ_ERR_INVALID_ARG
+    assert call(sb=-64) == bq.BQ_ERR_INVALID_ARG
+    assert call(sc=32 * 64 - 8) == bq.BQ_ERR_INVALID_ARG          # outputs would overlap
+    assert call(sc=0) == bq.BQ_ERR_INVALID_ARG
+    assert call(sa=40) == bq.BQ_ERR_ALIGNMENT                     # 40-byte item offsets
+    assert call(scs=12) == bq.BQ_ERR_ALIGNMENT                    # 24-byte scale offsets
+    assert call(sb=1 << 62) == bq.BQ_ERR_UNSUPPORTED               # saturated, no overflow
+    assert call(batch=(1 << 16) + 1) == bq.BQ_ERR_UNSUPPORTED
+    assert call(act=5) == bq.BQ_ERR_INVALID_ARG
+    assert call(K=96) == bq.BQ_ERR_UNSUPPORTED
+    assert call(batch=0, C=None, A=None) == bq.BQ_OK              # empty batch
+    assert call(M=0) == bq.BQ_OK
+    g = lib.bq_gemm_f16xi4_batched
+    assert g(FAKE, 0, FAKE, 2048, 1, 2, 4, 64, 64, None, 0, 0, FAKE, 256, None) == bq.BQ_ERR_INVALID_ARG  # scale required
+    assert g(FAKE, 0, FAKE, 2048, 1, 2, 0, 64, 64, FAKE, 64, 0, FAKE, 0, None) == bq.BQ_OK
 
 
 def test_device_status_null(lib):

@@ -271,6 +271,48 @@ def test_f16xi4_activation(act, M, N, K):
                      f16_ulps=1 if act == "gelu" else 0)
 
 
+# ---------------------------------------------------------------------------
+# batched GEMMs with broadcast operands (the fused QKV projection: one block
+# of activations, three stacked weight matrices)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("bits", [8, 4, 2])
+@pytest.mark.parametrize("M", [1, 40, 300])
+def test_batched_shared_activations(bits, M):
+    rng = np.random.default_rng(100 + bits + M)
+    N, K, nb = 192, 256, 3
+    A = W.int8_uniform(rng, (1, M, K))
+    Bq = [_codes(rng, bits, (N, K)) for _ in range(nb)]
+    sw = W.uniform_f16(rng, (nb, N), 1e-3, 1e-2)
+    sx = W.uniform_f16(rng, (M,), 1e-3, 1e-1)
+    if bits == 8:
+        Bw = dev(np.stack(Bq))
+        y = host(bq.bq_gemm_i8xi8_batched(dev(A), Bw, row_scale=dev(sx), col_scale=dev(sw), activation="relu"))
+        c = host(bq.bq_gemm_i8xi8_batched(dev(A), Bw))
+    else:
+        Bw = dev(np.stack([O.pack(b, bits, "interleaved") for b in Bq]))
+        fn = bq.bq_gemm_i8xi4_batched if bits == 4 else bq.bq_gemm_i8xi2_batched
+        y = host(fn(dev(A), Bw, "interleaved", row_scale=dev(sx), col_scale=dev(sw), activation="relu"))
+        c = host(fn(dev(A), Bw, "interleaved"))
+    for b in range(nb):
+        c_ref = O.gemm_int(A[0], Bq[b])
+        assert (c[b] == c_ref).all(), f"item {b}"
+        assert_f16_close(y[b], O.dequant(c_ref, sw[b], sx, act="relu"), sx[:, None].astype(np.float64) * sw[b][None, :],
+                         f"item {b}")
+
+
+def test_batched_shared_weights_f16xi4():
+    rng = np.random.default_rng(7)
+    nb, M, N, K = 4, 20, 320, 512
+    X = W.normal_f16(rng, (nb, M, K), 1.0)
+    q = W.int4_uniform(rng, (N, K))
+    s = W.uniform_f16(rng, (N,), 0.008, 0.016)
+    Wp = dev(O.pack(q, 4, "interleaved")[None])
+    y = host(bq.bq_gemm_f16xi4_batched(dev(X), Wp, dev(s), activation="gelu"))
+    for b in range(nb):
+        assert_f16_close(y[b], O.gemm_f16xq(X[b], q, s, act="gelu"), s[None, :].astype(np.float64), f"item {b}",
+                         f16_ulps=1)
+
+
 def test_activation_none_matches_plain_call():
     rng = np.random.default_rng(11)
     A = W.int8_uniform(rng, (64, 256))
