@@ -461,7 +461,17 @@ def measure_paths(torch, bq, W, roofline, dev, flush, stream, hbm_peak, tc_peak,
         ms = med(lambda: bq.bq_gemm_i8xi4_act(A2, B2, act, "interleaved", col_scale=s2, out=C2))
         out[f"i8xi4_{act}_4096^3"] = {"ms": ms, "TOPS": OPS2 / (ms * 1e-3) / 1e12,
                                       "tc_frac": OPS2 / (ms * 1e-3) / 1e12 / tc_peak}
-    del A2, B2, s2, C2
+    # batched with a shared activation block: one 1024 x 4096 A against three stacked 4096 x 4096 int4
+    # weights (a fused QKV projection), each item with its own column scales
+    Aq = A2[:1024].unsqueeze(0).contiguous()
+    Bq3 = torch.stack([B2, torch.roll(B2, 977, 0), torch.roll(B2, 1931, 0)]).contiguous()
+    sq = torch.stack([s2, s2, s2]).contiguous()
+    Cq = torch.empty((3, 1024, 4096), dtype=torch.float16, device=dev)
+    ms = med(lambda: bq.bq_gemm_i8xi4_batched(Aq, Bq3, "interleaved", col_scale=sq, out=Cq))
+    ops = 3 * roofline.matmul_ops(1024, 4096, 4096)
+    out["qkv_i8xi4_batched_3x1024x4096x4096"] = {"ms": ms, "TOPS": ops / (ms * 1e-3) / 1e12,
+                                                 "tc_frac": ops / (ms * 1e-3) / 1e12 / tc_peak}
+    del A2, B2, s2, C2, Aq, Bq3, sq, Cq
     # fp16 x INT4, dynamic M
     d3 = W.cfg3(M=1024, source=False)
     W3 = bq.bq_pack_weights(torch.from_numpy(d3["W"]).to(dev), 4, "interleaved")
