@@ -73,3 +73,20 @@ def test_reference_arm_runs_on_rank_zero_only():
     with contextlib.redirect_stdout(out):
         assert bench.run_reference(A, rank=1, world=2) is None
     assert out.getvalue() == ""
+
+
+def test_binding_batch_strides():
+    """Host-side stride logic of the batched binding (no GPU): a leading
+    dimension of 1 broadcasts (stride 0), a 1-D scale vector is shared."""
+    import torch
+    import quantized_mixed_precision_gb300 as bq
+    a1 = torch.zeros((1, 4, 64), dtype=torch.int8)
+    a3 = torch.zeros((3, 4, 64), dtype=torch.int8)
+    assert bq._batch_stride(a1, 3, "A") == 0
+    assert bq._batch_stride(a3, 3, "A") == 4 * 64
+    with pytest.raises(ValueError):
+        bq._batch_stride(torch.zeros((2, 4, 64)), 3, "A")
+    assert bq._scale_stride(None, 3, "s") == 0
+    assert bq._scale_stride(torch.zeros((64,)), 3, "s") == 0
+    assert bq._scale_stride(torch.zeros((1, 64)), 3, "s") == 0
+    assert bq._scale_stride(torch.zeros((3, 64)), 3, "s") == 64
