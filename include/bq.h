@@ -123,7 +123,7 @@ bq_status bq_pack_weights(const int8_t* q, int64_t n, int64_t k, int bits, int l
  *   [BitBLAS 混合精度算子开发实战 1 and 2; 案例1; BMINF igemm and
  *    elementwise_copy_scale]
  *
- *   Cint[i, j] = sum_k int(A[i, k]) * int(B[j, k])        (exact)
+ *   Cint[i, j] = sum_k int(A[i, k]) * int(B[j, k])        (exact, on every path)
  *   If row_scale == NULL and col_scale == NULL:  C is int32 (M, N), C = Cint.
  *   Otherwise C is fp16 (M, N):
  *     C[i, j] = fp16_rne( float(Cint[i, j]) * float(col_scale[j]) [* float(row_scale[i])] )
@@ -140,10 +140,20 @@ bq_status bq_pack_weights(const int8_t* q, int64_t n, int64_t k, int bits, int l
  *   sum stays within 2**24 and the fp32 tensor-core accumulation is exact;
  *   for i8xi2 |a * b| <= 256 and K <= 65536 already guarantees that).
  *   With K == 0 the output is all zeros and A / B may be NULL.
+ *   The tensor cores multiply exact fp16 images of the codes into fp32
+ *   accumulators, which hold integers exactly up to 2**24: every fp32 chain
+ *   is kept within that bound, so the fp16 epilogue starts from the exact
+ *   Cint as well.  int8 x int8 products reach 2**14, so its chains are at
+ *   most 1024 k long: CTA pairs drain the accumulator every 15 k-blocks
+ *   (its high part collects as an integer in the output's own bytes before
+ *   the epilogue overwrites them), the single-CTA kernel uses separate TMEM
+ *   slices or split-K ranges of at most 16 k-blocks summed as integers.
  *   Any M >= 0.  Dispatch: M <= 16 runs the skinny kernel (one pass over the
  *   weights; int8 x int8 uses an exact dp4a kernel there), larger M the
  *   tensor-core GEMM: 256-row tiles on CTA pairs when the grid fills the GPU,
- *   128-row tiles with K split over a cluster otherwise.
+ *   128-row tiles with K split over a cluster otherwise.  int8 x int8 shapes
+ *   with no exact tensor-core configuration (fp16 output with K > 8192 on
+ *   CTA pairs, K > 4096 on grids smaller than the GPU) run the dp4a kernel.
  *   Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA.
  */
 bq_status bq_gemm_i8xi8(const int8_t* A, const int8_t* B, int64_t M, int64_t N, int64_t K,
@@ -250,10 +260,14 @@ bq_status bq_gemm_f16xi4_batched(const uint16_t* X, int64_t stride_x, const uint
  * reports BQ_OK because it is asynchronous.
  *
  * bq_device_status: synchronises the device, returns the recorded status in
- *   *status_out (BQ_OK if none) and clears it when reset != 0.
+ *   *status_out (BQ_OK if none) and clears it when reset != 0.  A value of
+ *   64 records a failed internal self-check (an output span outside the
+ *   output, skipped rather than accessed): a library defect, not a caller
+ *   error.
  * bq_set_wait_timeout_ns: sets the time limit of those waits for later
  *   launches (default 2 s).  Returns the previous value.  Intended for tests
- *   that make a wait run out (a limit of 0 gives up at the first poll).
+ *   that make a wait run out: with a limit of 0 every wait whose phase has
+ *   not completed at its first (non-blocking) poll gives up.
  */
 bq_status bq_device_status(int* status_out, int reset);
 int64_t bq_set_wait_timeout_ns(int64_t ns);

@@ -63,7 +63,8 @@ bq_status run_gemm(GemmArgs g, void* stream) {
   }
   cudaError_t e;
   if (g.act == ACT_I8 && g.bbits == 8) {
-    const bool tc_ok = g.M > SKINNY_M && (g.epi != EPI_I32 || g.K <= 4096);
+    // skinny M, and shapes with no exact tensor-core configuration, use dp4a
+    const bool tc_ok = g.M > SKINNY_M && gemm_tc_i8_exact(g);
     e = tc_ok ? launch_gemm_tc(g, s) : launch_gemm_dp4a(g, s);
   } else if (gemm_swap_applies(g)) {
     e = launch_gemm_swap(g, s);

@@ -157,6 +157,8 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
+// One blocking poll: try_wait may suspend the thread until the phase
+// completes, for up to a hardware-defined time.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -169,17 +171,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One non-blocking poll: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed, or give up after
 // timeout_ns nanoseconds: records BQ_ERR_TIMEOUT in *status, returns false.
+// The first poll does not block and the deadline is checked before every
+// blocking poll, so a zero limit gives up unless the phase had completed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 >= timeout_ns) {
       record_error(status, BQ_ERR_TIMEOUT);
       return false;
     }
+    if (mbar_try_wait(bar, parity)) return true;
   }
 }
 
@@ -295,16 +312,29 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-// Bounded wait (acquire at cluster scope) for arrivals made by peer CTAs.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait (acquire at cluster scope) for arrivals made by peer CTAs;
+// same polling as mbar_wait.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int* status) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
+  if (mbar_test_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
     if (globaltimer_ns() - t0 >= timeout_ns) {
       record_error(status, BQ_ERR_TIMEOUT);
       return false;
     }
+    if (mbar_try_wait_cluster(bar, parity)) return true;
   }
 }
 
@@ -317,6 +347,24 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// Release a TMA-filled shared-memory stage right after reading it with
+// ordinary loads, without a fence: `dep` folds every word the thread loaded
+// from the stage and `zero` is a run-time zero the compiler cannot see
+// through, so the arrival count 1 + (dep & zero) is a data dependency of the
+// arrive on every load.  The arrive cannot issue before all of them have
+// returned their data, so the TMA refill it allows cannot overtake them (an
+// mbarrier release alone does not order generic-proxy reads before an
+// async-proxy write).
+__device__ __forceinline__ void mbar_arrive_after_loads(uint64_t* bar, uint32_t dep, uint32_t zero) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+               "r"(1u + (dep & zero))
+               : "memory");
+}
+
+// XOR of the four words of a 16-byte value (folded into `dep` above).
+__device__ __forceinline__ uint32_t fold4(const uint4& v) { return v.x ^ v.y ^ v.z ^ v.w; }
+
 
 // ---------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor core) wrappers, cta_group::1
@@ -452,9 +500,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
 
 // Arrive once on an mbarrier when all previously issued tcgen05 ops of this thread complete.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -476,8 +521,37 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_ld_wait() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// tcgen05.ld and tcgen05.st are asynchronous: the load writes its destination
+// registers, and the store reads its source registers, some time after issue.
+// Every wait below names those registers as operands, so that the compiler
+// neither reads the destinations before the load has written them nor
+// reuses the sources' physical registers while the store may still read
+// them (an untied wait left both open, and stores then read registers the
+// compiler had already reassigned).
+//
+// Wait for this thread's tcgen05.ld and tie the 32 destination registers to
+// the wait, so that no use of them (nor any reuse of their physical
+// registers) is scheduled before the asynchronous load has written them.
+__device__ __forceinline__ void tmem_ld_wait_tied(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+        "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+        "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+        "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
+
+// Wait for this thread's tcgen05.st with its 32 source registers as inputs of
+// the wait: they stay allocated, unchanged, until the store has read them.
+__device__ __forceinline__ void tmem_st_wait_tied(const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::st.sync.aligned;" ::"r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+      "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile stored in the

@@ -23,6 +23,10 @@ cudaError_t launch_quantize(const void* x, int xtype, int64_t rows, int64_t cols
 cudaError_t launch_pack(const int8_t* q, int64_t n, int64_t k, int bits, int layout, uint8_t* packed,
                         cudaStream_t stream);
 
+// Device status recorded by a failed internal self-check (a library defect,
+// not a caller error): an output span outside the output's bounds.
+constexpr int BQ_DIAG_RANGE = 64;
+
 // Epilogue kinds shared by the GEMM kernels.
 enum EpiKind : int { EPI_I32 = 0, EPI_F16_COL = 1, EPI_F16_ROWCOL = 2 };
 // Activation operand kinds.
@@ -63,6 +67,9 @@ cudaError_t launch_gemv_mma(const GemmArgs& g, cudaStream_t stream);
 cudaError_t launch_gemm_dp4a(const GemmArgs& g, cudaStream_t stream);
 // Tensor-core (tcgen05) GEMM for larger M.
 cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream);
+// Whether launch_gemm_tc has an exact configuration for int8 x int8 (CTA
+// pairs with chunked accumulation, or single-CTA chains of <= 16 k-blocks).
+bool gemm_tc_i8_exact(const GemmArgs& g);
 // CTA-pair tensor-core kernel (int8 activations): the tile width it would use
 // for this problem, or 0 when the single-CTA kernel is the better fit.
 int gemm_pair_bn(const GemmArgs& g);

@@ -42,6 +42,19 @@
 // One CTA per SM (the shared-memory footprint guarantees it), so a CTA's
 // collective tensor-memory allocation never waits on another pair that holds
 // the same SM's tensor memory.
+//
+// Chunked accumulation (DR, int8 x int8 with K > 1024).  A product of two
+// int8 codes reaches 2**14, so one 64-k block adds up to 2**20 and an fp32
+// chain of more than 16 blocks may pass 2**24, where odd integers are no
+// longer representable.  In DR mode the MMA issuer commits the end of every
+// chunk of CH_KB = 15 k-blocks; each consumer warp then reads its part of the
+// accumulator D (exact), splits it as D = 8192 h + L with h = rint(D / 8192),
+// writes L (|L| <= 4096) back into tensor memory and arrives; only then are
+// the next chunk's MMAs issued, on top of L, so every partial sum stays below
+// 4096 + 15 * 2**20 < 2**24.  The high parts h accumulate as integers in the
+// output's own bytes (int16 per element for fp16 outputs, int32 for int32
+// outputs; every element belongs to one thread of one CTA), and the epilogue
+// forms Cint = 8192 * sum(h) + rint(D) exactly before the dequantisation.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -62,6 +75,8 @@ constexpr int P_BW = 2;                  // warps per weight converter group
 constexpr int P_A_WARPS = 4 * P_NA;
 constexpr int P_B_THREADS = P_BW * 32;   // weight converters per group
 constexpr uint64_t P_DRAIN_NS = 4000000000ull;
+constexpr int CH_KB = 15;                // k-blocks per accumulation chunk (DR mode)
+constexpr float H_UNIT = 8192.0f;        // weight of one high-part unit (2**13)
 
 // AF16: fp16 activations, loaded by TMA straight into the MMA's 128B-swizzled
 // K-major layout (no activation converters, A read from shared memory), and
@@ -118,17 +133,114 @@ struct PairCfg {
   // parity of a phase two behind, which needs n <= ST.
   static_assert(P_NA <= ST && NB <= ST, "converter groups per stage ring");
   static_assert(CONSUMER_WARPS * STG_BYTES <= OFF_BAR, "epilogue staging fits in the pipeline buffers");
+  static_assert((3 * ST + 2 * RST + 3) * 8 + 4 <= 256, "barrier area");
 };
+
+// True if the 32 consecutive output elements at element offset `off` lie
+// inside the M x N output; otherwise records BQ_DIAG_RANGE (a self-check of
+// the chunked accumulation's bookkeeping) and the caller skips the access.
+__device__ __forceinline__ bool out_span_ok(size_t off, int M, int N, int* status) {
+  if (off % 32 == 0 && off + 32 <= (size_t)M * (size_t)N) return true;
+  record_error(status, BQ_DIAG_RANGE);
+  return false;
+}
+
+// DR: one consumer warp's drain of chunk boundary b (the accumulator after
+// k-block CH_KB * b - 1).  The warp covers its TMEM lane quadrant (tile rows
+// 32q .. 32q + 31) and its (at most two) 32-column chunks, the same rows and
+// columns it stores in the epilogue: it splits every accumulator value as
+// D = 8192 h + L, writes L back, arrives on the even CTA's drained barrier
+// and then adds h to the running high parts in the output's bytes (int16 for
+// fp16 outputs, int32 for int32 outputs).  False if a wait gave up.
+template <int BN, int PARTS>
+__device__ __forceinline__ bool pair_drain(int b, uint32_t tmem, uint64_t* chunk_bar, uint64_t* drained_bar, int warp,
+                                        int lane, int m0, int n0, int M, int N, int epi, void* out,
+                                        uint64_t timeout_ns, int* status) {
+  const int q = warp & 3, part = warp >> 2;
+  const int row0 = m0 + 32 * q, row = row0 + lane;
+  if (!__all_sync(0xffffffffu, mbar_wait(chunk_bar, (uint32_t)((b - 1) & 1), timeout_ns, status))) return false;
+  tc_fence_after();
+  uint32_t hp[2][16];   // high parts, two int16 per word
+  bool live[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int ch = part + j * PARTS;
+    live[j] = ch < BN / 32 && n0 + 32 * ch < N && row0 < M;   // warp-uniform
+    if (live[j]) {
+      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * ch);
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(ta, r);
+      tmem_ld_wait_tied(r);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        // D = 8192 h + L exactly: D is an integer below 2**24, h = rint(D / 8192), |L| <= 4096
+        const float f0 = __uint_as_float(r[2 * i]), f1 = __uint_as_float(r[2 * i + 1]);
+        const float h0 = rintf(f0 * (1.0f / H_UNIT)), h1 = rintf(f1 * (1.0f / H_UNIT));
+        r[2 * i] = __float_as_uint(fmaf(-H_UNIT, h0, f0));
+        r[2 * i + 1] = __float_as_uint(fmaf(-H_UNIT, h1, f1));
+        hp[j][i] = ((uint32_t)(int)h0 & 0xffffu) | ((uint32_t)(int)h1 << 16);
+      }
+      tmem_st_32x32b_x32(ta, r);
+      tmem_st_wait_tied(r);
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(drained_bar), 0));
+  if (row >= M) return true;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    if (!live[j]) continue;
+    const size_t off = (size_t)row * N + n0 + 32 * (part + j * PARTS);
+    if (!out_span_ok(off, M, N, status)) continue;
+    if (epi == EPI_I32) {
+      int4* p = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + off);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const uint32_t w0 = hp[j][2 * v], w1 = hp[j][2 * v + 1];
+        int4 h = make_int4((int)(int16_t)(w0 & 0xffffu), (int)w0 >> 16, (int)(int16_t)(w1 & 0xffffu), (int)w1 >> 16);
+        if (b > 1) {
+          const int4 o = p[v];
+          h.x += o.x;
+          h.y += o.y;
+          h.z += o.z;
+          h.w += o.w;
+        }
+        p[v] = h;
+      }
+    } else {
+      uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + off);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint4 h = make_uint4(hp[j][4 * v], hp[j][4 * v + 1], hp[j][4 * v + 2], hp[j][4 * v + 3]);
+        if (b > 1) {
+          const uint4 o = p[v];
+          h.x = __vadd2(h.x, o.x);
+          h.y = __vadd2(h.y, o.y);
+          h.z = __vadd2(h.z, o.z);
+          h.w = __vadd2(h.w, o.w);
+        }
+        p[v] = h;
+      }
+    }
+  }
+  return true;
+}
 
 // ACTV: the fp16 epilogue applies the activation in bits 4.. of `epi` (a
 // separate instantiation, so the kernel without one carries no trace of it).
-template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool ACTV>
+// DR: chunked accumulation (int8 x int8, K > 1024); `out` is the output
+// (also the home of the running high parts), used only in that mode.
+template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool ACTV, bool DR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST, AF16>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, int M, int N, int K,
                      const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
-                     uint64_t timeout_ns, int* status) {
+                     void* out, uint64_t timeout_ns, int* status) {
   using C = PairCfg<BBITS, BN, ST, RST, AF16>;
+  static_assert(!DR || (BBITS == 8 && !AF16), "chunked accumulation is for int8 x int8");
+  // DR: each consumer warp drains at most two 32-column chunks of its quadrant
+  static_assert(!DR || BN / 32 <= 2 * (C::CONSUMER_WARPS / 4), "drain chunks per warp");
   const int actfn = epi >> 4;
   epi &= 15;
   extern __shared__ uint8_t smem_raw[];
@@ -140,7 +252,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
   uint64_t* rempty_bar = rfull_bar + RST;                                // raw stage read
   uint64_t* accum_bar = rempty_bar + RST;                                // all MMAs done
   uint64_t* afull_bar = accum_bar + 1;                                   // fp16 activation tile landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(afull_bar + ST);
+  uint64_t* chunk_bar = afull_bar + ST;                                  // DR: MMAs of a chunk done
+  uint64_t* drained_bar = chunk_bar + 1;                                 // DR (even CTA): chunk drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained_bar + 1);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -149,6 +263,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
   const int n0 = blockIdx.y * BN;                                      // the pair's output columns
   const int nb0 = n0 + (int)rank * C::HB;                              // this CTA's weight rows
   const int nkb = K / PK;
+  const int ndr = DR ? (nkb - 1) / CH_KB : 0;   // chunk boundaries inside K (DR)
+  const uint32_t rzero = (uint32_t)K >> 30;      // 0 (K <= 65536), not known to the compiler
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -161,6 +277,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       mbar_init(&rempty_bar[s], C::RAW_READERS);   // every group that reads a raw stage releases it once
     }
     mbar_init(accum_bar, 1);
+    mbar_init(chunk_bar, 1);
+    mbar_init(drained_bar, 2 * C::CONSUMER_WARPS);   // one arrival per consumer warp of each CTA
     mbar_fence_init();
   }
   if (warp == C::MMA_WARP) {
@@ -179,6 +297,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
   cluster_sync_all();
 
   bool ok = true;
+  int db = 1;   // DR: next chunk boundary this warp drains
+  // DR: before a consumer writes the stage of k-block kb, it drains every
+  // boundary that the MMAs of kb - ST (the stage's previous use) lie behind.
+  // By then it has converted all of its k-blocks of the drained chunk, so the
+  // chunk's MMAs never wait for it, and the ST stages after a boundary are
+  // already converted when the MMAs resume.
+  auto drain_before = [&](int kb) -> bool {
+    if constexpr (DR) {
+      while (db <= ndr && kb >= db * CH_KB + ST) {
+        if (!pair_drain<BN, C::CONSUMER_WARPS / 4>(db, tmem, chunk_bar, drained_bar, warp, lane, m0, n0, M, N, epi,
+                                                   out, timeout_ns, status))
+          return false;
+        ++db;
+      }
+    }
+    return true;
+  };
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -226,6 +361,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       const int kb_half = C::NACC == 2 ? (nkb + 1) / 2 : nkb;
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % ST;
+        if (DR && kb > 0 && kb % CH_KB == 0) {
+          // the next chunk adds on top of the drained accumulator (both CTAs' consumer warps)
+          const int b = kb / CH_KB;
+          if (!__all_sync(0xffffffffu, mbar_wait_cluster(drained_bar, (b - 1) & 1, timeout_ns, status))) break;
+        }
         if (!__all_sync(0xffffffffu, mbar_wait_cluster(&full_bar[s], (kb / ST) & 1, timeout_ns, status))) break;
         tc_fence_after();
         const int slice = kb < kb_half ? 0 : 1;
@@ -245,6 +385,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
               tc_mma_f16_ts_pair(d, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
           }
           tc_commit_pair(&empty_bar[s], 0x3);
+          // DR: the last k-block of a chunk (with more to come): let the consumers drain
+          if (DR && (kb + 1) % CH_KB == 0 && kb + 1 < nkb) tc_commit_pair(chunk_bar, 0x3);
         }
         __syncwarp();
       }
@@ -260,6 +402,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
     const int q = warp & 3;                               // TMEM lane quadrant
     const int r = q * 32 + lane;                          // tile row == TMEM lane
     for (int kb = warp >> 2; kb < nkb; kb += P_NA) {
+      if (!drain_before(kb)) {
+        ok = false;
+        break;
+      }
       const int grp = kb / C::RKB, rs = grp % RST;
       // the group's first k-block of a raw stage waits for it to land
       if (kb % C::RKB < P_NA && !warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
@@ -272,7 +418,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       uint4 v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(box + (((c0 + j) ^ (r & 7)) << 4));
-      if ((kb % C::RKB) + P_NA >= C::RKB || kb + P_NA >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
+      if ((kb % C::RKB) + P_NA >= C::RKB || kb + P_NA >= nkb)   // group's last use
+        mbar_arrive_after_loads(&rempty_bar[rs], fold4(v[0]) ^ fold4(v[1]) ^ fold4(v[2]) ^ fold4(v[3]), rzero);
       uint32_t h[32];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -286,8 +433,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         ok = false;
         break;
       }
+      // order the store after the MMAs whose completion the barrier reported:
+      // without the fence it may overwrite the stage while they still read it
+      tc_fence_after();
       tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::ACC_COLS + s * C::A_COLS), h);
-      tmem_st_wait();
+      tmem_st_wait_tied(h);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&full_bar[s]), 0));
@@ -298,6 +448,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
     const int bw = warp - C::A_WARPS;
     const int c = (bw % P_BW) * 32 + lane;                // converter thread within its group
     for (int kb = bw / P_BW; kb < nkb; kb += C::NB) {
+      if (!drain_before(kb)) {
+        ok = false;
+        break;
+      }
       const int grp = kb / C::RKB, rs = grp % RST;
       if (kb % C::RKB < C::NB && !warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
         ok = false;
@@ -316,7 +470,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         v[i] = pi < C::B_PIECES ? *reinterpret_cast<const uint4*>(raw + r * C::B_BOX_X + (pos << 4))
                                 : make_uint4(0, 0, 0, 0);
       }
-      if ((kb % C::RKB) + C::NB >= C::RKB || kb + C::NB >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
+      if ((kb % C::RKB) + C::NB >= C::RKB || kb + C::NB >= nkb) {   // group's last use
+        uint32_t dep = 0;
+#pragma unroll
+        for (int i = 0; i < C::NPB; ++i) dep ^= fold4(v[i]);
+        mbar_arrive_after_loads(&rempty_bar[rs], dep, rzero);
+      }
       const int s = kb % ST;
       if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) {
         ok = false;
@@ -341,6 +500,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 
   // ------------------------------------------------------------ epilogue (consumer warps)
   if (warp < C::CONSUMER_WARPS) {
+    if constexpr (DR) {
+      // boundaries no k-block of this warp lay behind
+      while (ok && db <= ndr) {
+        ok = pair_drain<BN, C::CONSUMER_WARPS / 4>(db, tmem, chunk_bar, drained_bar, warp, lane, m0, n0, M, N, epi,
+                                                   out, timeout_ns, status);
+        ++db;
+      }
+    }
     const bool acc_ok = warp_wait(accum_bar, 0, ok ? timeout_ns : 0, status);
     tc_fence_after();
     if (acc_ok) {
@@ -362,13 +529,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         if (ncol >= N) break;
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
-        tmem_ld_wait();
+        tmem_ld_wait_tied(r);
         if constexpr (C::NACC == 2) {
           uint32_t r2[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(col + BN), r2);
-          tmem_ld_wait();
+          tmem_ld_wait_tied(r2);
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+        }
+        // exact integer sums: rint(D), plus 8192 times the drained high parts (DR)
+        int ci[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ci[i] = __float2int_rn(__uint_as_float(r[i]));
+        if constexpr (DR) {
+          const size_t off = (size_t)row * N + ncol;
+          if (row < M && out_span_ok(off, M, N, status)) {
+            if (epi == EPI_I32) {
+              const int4* p = reinterpret_cast<const int4*>(static_cast<const int32_t*>(out) + off);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const int4 h = p[v];
+                ci[4 * v] += h.x * (int)H_UNIT;
+                ci[4 * v + 1] += h.y * (int)H_UNIT;
+                ci[4 * v + 2] += h.z * (int)H_UNIT;
+                ci[4 * v + 3] += h.w * (int)H_UNIT;
+              }
+            } else {
+              const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(out) + off);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const uint4 h = p[v];
+                const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  ci[8 * v + 2 * e] += (int)(int16_t)(w[e] & 0xffffu) * (int)H_UNIT;
+                  ci[8 * v + 2 * e + 1] += ((int)w[e] >> 16) * (int)H_UNIT;
+                }
+              }
+            }
+          }
+          // the fp16 dequantisation starts from the exact sum (one rounding to fp32)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__int2float_rn(ci[i]));
         }
         if (lane == 0) bulk_wait_read_all();   // the previous box has left the staging buffer
         __syncwarp();
@@ -377,9 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             *reinterpret_cast<int4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                make_int4(__float2int_rn(__uint_as_float(r[4 * j])), __float2int_rn(__uint_as_float(r[4 * j + 1])),
-                          __float2int_rn(__uint_as_float(r[4 * j + 2])),
-                          __float2int_rn(__uint_as_float(r[4 * j + 3])));
+                make_int4(ci[4 * j], ci[4 * j + 1], ci[4 * j + 2], ci[4 * j + 3]);
         } else {
           uint32_t hv[16];
 #pragma unroll
@@ -405,6 +605,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
                 make_uint4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]);
         }
         fence_proxy_async_smem();   // generic stores -> visible to the TMA engine
+        // DR: this box's high parts were written and read through the generic
+        // proxy; order those accesses before the TMA store of the same bytes
+        if constexpr (DR) asm volatile("fence.proxy.async.global;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
           tma_store_2d(&tmap_c, stg, ncol, row0);   // rows past M are not written
@@ -429,7 +632,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool ACTV>
+template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool ACTV, bool DR>
 cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   using C = PairCfg<BBITS, BN, ST, RST, AF16>;
   int* status = nullptr;
@@ -450,22 +653,28 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   else
     e = make_map(&mc, g.c, 2, (uint64_t)g.N, (uint64_t)g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, AF16, ACTV>;
+  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, AF16, ACTV, DR>;
   e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(2 * ((g.M + 2 * PM - 1) / (2 * PM))), (unsigned)((g.N + BN - 1) / BN));
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(ma, mb, mc, (int)g.M, (int)g.N, (int)g.K,
                                               reinterpret_cast<const __half*>(g.row_scale),
-                                              reinterpret_cast<const __half*>(g.col_scale), epi_arg(g),
+                                              reinterpret_cast<const __half*>(g.col_scale), epi_arg(g), g.c,
                                               (uint64_t)wait_timeout_ns(), status);
   return cudaGetLastError();
 }
 
 template <int BBITS, int BN, int ST, int RST, bool AF16, bool ACTV>
 cudaError_t launch_pair_act(const GemmArgs& g, cudaStream_t stream) {
-  if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN)
-    return launch_pair_t<BBITS, BN, false, ST, RST, AF16, ACTV>(g, stream);
-  return launch_pair_t<BBITS, BN, true, ST, RST, AF16, ACTV>(g, stream);
+  if constexpr (BBITS == 8 && !AF16) {
+    // int8 x int8 beyond 16 k-blocks: chunked accumulation keeps the sums exact
+    if (g.K > 16 * PK) return launch_pair_t<8, BN, true, ST, RST, false, ACTV, true>(g, stream);
+    return launch_pair_t<8, BN, true, ST, RST, false, ACTV, false>(g, stream);
+  } else {
+    if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN)
+      return launch_pair_t<BBITS, BN, false, ST, RST, AF16, ACTV, false>(g, stream);
+    return launch_pair_t<BBITS, BN, true, ST, RST, AF16, ACTV, false>(g, stream);
+  }
 }
 
 template <int BBITS, int BN, int ST, int RST, bool AF16 = false>
@@ -502,8 +711,10 @@ int gemm_pair_bn(const GemmArgs& g) {
   if (g.M <= 0 || g.N <= 0 || g.K < PK) return 0;
   // fp16 activations accumulate two halves of K separately: at least two k-blocks
   if (g.act == ACT_F16 && (g.bbits != 4 || g.K < 2 * PK)) return 0;
-  // int32 outputs with int8 weights accumulate exactly in one fp32 chain only up to K = 1024
-  if (g.bbits == 8 && g.epi == EPI_I32 && g.K > 1024) return 0;
+  // int8 x int8 beyond K = 1024 runs with chunked accumulation, whose running
+  // high parts live in the output: as int16 for fp16 outputs, where
+  // |sum of high parts| <= 2K + 2048 must stay below 2**15
+  if (g.bbits == 8 && g.epi != EPI_I32 && g.K > 8192) return 0;
   if (g.bbits != 8 && g.bbits != 4 && g.bbits != 2) return 0;
   // grids smaller than the GPU go to the single-CTA kernel, which splits K over clusters
   const long long tiles1 = ((g.N + 255) / 256) * ((g.M + 127) / 128);

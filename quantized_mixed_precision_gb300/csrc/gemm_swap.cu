@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
   const int warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * SW_N;
   const int nkb = K / SW_K;
+  const uint32_t rzero = (uint32_t)K >> 30;   // 0 (K <= 65536), not known to the compiler
   // k-blocks [0, kb_half) accumulate into slice 0, the rest into slice 1
   const int kb_half = nkb >= 2 ? (nkb + 1) / 2 : nkb;
   const bool two_slices = kb_half < nkb;
@@ -214,7 +215,8 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
         const int c0 = (kb % C::RKB) * 2;                 // two 16-byte chunks of a 128-byte row
         const uint4 v0 = *reinterpret_cast<const uint4*>(rowp + ((c0 ^ (r & 7)) << 4));
         const uint4 v1 = *reinterpret_cast<const uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4));
-        if ((kb % C::RKB) + SW_NG >= C::RKB || kb + SW_NG >= nkb) mbar_arrive(&rempty_bar[rs]);
+        if ((kb % C::RKB) + SW_NG >= C::RKB || kb + SW_NG >= nkb)
+          mbar_arrive_after_loads(&rempty_bar[rs], fold4(v0) ^ fold4(v1), rzero);
         const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -228,7 +230,8 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
       } else {
         const int c0 = kb % C::RKB;                       // one 16-byte chunk of a 64-byte row (64B swizzle)
         const uint4 v0 = *reinterpret_cast<const uint4*>(rowp + ((c0 ^ ((r >> 1) & 3)) << 4));
-        if ((kb % C::RKB) + SW_NG >= C::RKB || kb + SW_NG >= nkb) mbar_arrive(&rempty_bar[rs]);
+        if ((kb % C::RKB) + SW_NG >= C::RKB || kb + SW_NG >= nkb)
+          mbar_arrive_after_loads(&rempty_bar[rs], fold4(v0), rzero);
         const uint32_t wv[4] = {v0.x, v0.y, v0.z, v0.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -243,8 +246,9 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
         ok = false;
         break;
       }
+      tc_fence_after();   // the store follows the MMAs that released the stage
       tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(2 * MN + s * C::A_COLS), h);
-      tmem_st_wait();
+      tmem_st_wait_tied(h);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&full_bar[s]);
@@ -260,11 +264,11 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
         for (int c = 0; c < MN / 32 + (MN % 32 ? 1 : 0); ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * c), v);
-          tmem_ld_wait();
+          tmem_ld_wait_tied(v);
           if (two_slices) {
             uint32_t v2[32];
             tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(MN + 32 * c), v2);
-            tmem_ld_wait();
+            tmem_ld_wait_tied(v2);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(v2[i]));
           }

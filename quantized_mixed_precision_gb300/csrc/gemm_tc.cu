@@ -13,9 +13,12 @@
 // tcgen05.mma kind::f16 into an fp32 accumulator in tensor memory.  Integer
 // products are exact and every partial sum is an integer; while those stay
 // below 2**24 the fp32 accumulation is exact too.  The host guarantees that
-// for the int32 paths by bounding K, or by splitting K into separately
-// accumulated TMEM slices of at most 1024 k that the epilogue sums as
-// integers.  fp16 activations accumulate in two slices (shorter fp32 chains).
+// for every integer path by bounding K, or (int8 x int8) by keeping every
+// chain at most 1024 k long: separately accumulated TMEM slices, or split-K
+// ranges of at most 16 k-blocks.  Slices and split-K partials of integer
+// operands are rounded to int32 and summed as integers before the epilogue,
+// so the fp16 dequantisation starts from the exact sum as well.  fp16
+// activations accumulate in two slices (shorter fp32 chains).
 //
 // One 128 x BN output tile per CTA; warp roles:
 //   producer warp  one thread issues 2-D TMA loads (cp.async.bulk.tensor) of
@@ -216,6 +219,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
   const int S = gridDim.z;
   const int kb_lo = (int)(((long long)blockIdx.z * (K / BK)) / S);
   const int nkb = (int)(((long long)(blockIdx.z + 1) * (K / BK)) / S) - kb_lo;
+  const uint32_t rzero = (uint32_t)K >> 30;      // 0 (K <= 65536), not known to the compiler
   // threads that consume one k-block: one A group (4 warps) and one B group (8 warps)
   constexpr int CONSUMERS = (C::A_WARPS / NG + 8) * 32;
 
@@ -341,7 +345,8 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
       uint4 v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(box + (((c0 + j) ^ (r & 7)) << 4));
-      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
+      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb)   // group's last use
+        mbar_arrive_after_loads(&rempty_bar[rs], fold4(v[0]) ^ fold4(v[1]) ^ fold4(v[2]) ^ fold4(v[3]), rzero);
       uint32_t h[32];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -352,8 +357,9 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
       }
       const int s = kb % ST;
       if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) break;
+      tc_fence_after();   // the store follows the MMAs that released the stage
       tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::ACC_COLS + s * C::A_COLS), h);
-      tmem_st_wait();
+      tmem_st_wait_tied(h);
       tc_fence_before();
       mbar_arrive(&full_bar[s]);
     }
@@ -381,7 +387,12 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
         v[i] = pi < C::B_PIECES ? *reinterpret_cast<const uint4*>(raw + r * C::B_BOX_X + (pos << 4))
                                 : make_uint4(0, 0, 0, 0);
       }
-      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb) mbar_arrive(&rempty_bar[rs]);   // group's last use
+      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb) {   // group's last use
+        uint32_t dep = 0;
+#pragma unroll
+        for (int i = 0; i < C::NPB; ++i) dep ^= fold4(v[i]);
+        mbar_arrive_after_loads(&rempty_bar[rs], dep, rzero);
+      }
       const int s = kb % ST;
       if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) {
         ok = false;
@@ -420,7 +431,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
 #pragma unroll
         for (int a = 0; a < NACC; ++a) {
           tmem_ld_32x32b_x32(taddr + a * BN, r);
-          tmem_ld_wait();
+          tmem_ld_wait_tied(r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float f = __uint_as_float(r[i]);
@@ -429,6 +440,11 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
           }
         }
         const int ncol = n0 + col;
+        // integer operands: the dequantisation starts from the exact integer sum of the slices
+        if (AMODE == A_I8_TMEM && NACC > 1) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __int2float_rn(iv[i]);
+        }
         if (row_ok && ncol < N) {
           if (epi == EPI_I32) {
             int4* dst = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + (size_t)row * N + ncol);
@@ -492,7 +508,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
           const int c = chalf * (NCH / 2) + cc;
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * c), v);
-          tmem_ld_wait();
+          tmem_ld_wait_tied(v);
           const uint32_t owner = (uint32_t)(c % S);
           const uint32_t row_addr = recv_base + (uint32_t)(((rank * slots + c / S) * BM + r) * 128);
 #pragma unroll
@@ -513,28 +529,44 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
         const int owned = (NCH - rank + S - 1) / S;
         for (int slot = chalf; slot < owned; slot += 2) {
           const int c = rank + slot * S;
+          // integer operands: every partial is an exact integer below 2**24, summed as int32
+          // (its float value for the fp16 epilogue is one rounding of the exact sum)
           float acc[32];
+          int iacc[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+          for (int i = 0; i < 32; ++i) {
+            acc[i] = 0.0f;
+            iacc[i] = 0;
+          }
           for (int src = 0; src < S; ++src) {
             const uint8_t* rowp = smem + ((src * slots + slot) * BM + r) * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const uint4 w4 = *reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4));
-              acc[4 * j] += __uint_as_float(w4.x);
-              acc[4 * j + 1] += __uint_as_float(w4.y);
-              acc[4 * j + 2] += __uint_as_float(w4.z);
-              acc[4 * j + 3] += __uint_as_float(w4.w);
+              const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if constexpr (AMODE == A_I8_TMEM) iacc[4 * j + e] += __float2int_rn(__uint_as_float(w[e]));
+                else acc[4 * j + e] += __uint_as_float(w[e]);
+              }
             }
+          }
+          if constexpr (AMODE == A_I8_TMEM) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = __int2float_rn(iacc[i]);
           }
           const int ncol = n0 + 32 * c;
           if (row_ok && ncol < N) {
             if (epi == EPI_I32) {
               int4* dst = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + (size_t)row * N + ncol);
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_int4(__float2int_rn(acc[4 * i]), __float2int_rn(acc[4 * i + 1]),
-                                   __float2int_rn(acc[4 * i + 2]), __float2int_rn(acc[4 * i + 3]));
+              for (int i = 0; i < 8; ++i) {
+                if constexpr (AMODE == A_I8_TMEM)
+                  dst[i] = make_int4(iacc[4 * i], iacc[4 * i + 1], iacc[4 * i + 2], iacc[4 * i + 3]);
+                else
+                  dst[i] = make_int4(__float2int_rn(acc[4 * i]), __float2int_rn(acc[4 * i + 1]),
+                                     __float2int_rn(acc[4 * i + 2]), __float2int_rn(acc[4 * i + 3]));
+              }
             } else {
               uint32_t hv[16];
 #pragma unroll
@@ -627,20 +659,35 @@ cudaError_t launch_layout(const GemmArgs& g, cudaStream_t stream) {
   return launch_t<AMODE, BBITS, BN, NACC, true, ST, RST, NG, MINB>(g, split, stream);
 }
 
+// int8 x int8 on the single-CTA kernel: the chains of at most 16 k-blocks
+// that keep the fp32 accumulation exact.  Returns the TMEM slices to use (1:
+// 256-wide tiles, K split over a cluster so that no CTA's range exceeds 16
+// k-blocks), or 0 when no configuration fits (K beyond 64 k-blocks).
+int tc_i8_slices(const GemmArgs& g) {
+  const int nkb = (int)(g.K / BK);
+  const long long tiles = ((g.N + 255) / 256) * ((g.M + BM - 1) / BM);
+  const int split = choose_split(tiles, nkb);
+  if ((nkb + split - 1) / split <= 16) return 1;
+  if (nkb <= 32) return 2;
+  if (nkb <= 64) return 4;
+  return 0;
+}
+
 }  // namespace
 
+bool gemm_tc_i8_exact(const GemmArgs& g) { return gemm_pair_bn(g) != 0 || tc_i8_slices(g) != 0; }
+
 cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream) {
-  const int nkb = (int)(g.K / BK);
   if (const int bn = gemm_pair_bn(g)) return launch_gemm_pair(g, bn, stream);
+  const int nkb = (int)(g.K / BK);
   if (g.act == ACT_I8 && g.bbits == 8) {
-    if (g.epi == EPI_I32) {
-      // int32 output: slices of at most 1024 k keep every partial sum < 2**24 exactly
-      if (nkb <= 16) return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 2>(g, stream);
-      if (nkb <= 32) return launch_layout<A_I8_TMEM, 8, 128, 2, 4, 2>(g, stream);
-      if (nkb <= 64) return launch_layout<A_I8_TMEM, 8, 64, 4, 4, 2, 1>(g, stream);
-      return cudaErrorInvalidValue;
+    // every fp32 chain at most 1024 k long: each partial sum < 2**24, exact
+    switch (tc_i8_slices(g)) {
+      case 1: return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 2>(g, stream);
+      case 2: return launch_layout<A_I8_TMEM, 8, 128, 2, 4, 2>(g, stream);
+      case 4: return launch_layout<A_I8_TMEM, 8, 64, 4, 4, 2, 1>(g, stream);
+      default: return cudaErrorInvalidValue;
     }
-    return launch_layout<A_I8_TMEM, 8, 256, 1, 4, 2>(g, stream);
   }
   // int8 activations with 4- / 2-bit weights: every partial sum < 2**24 (host-bounded K)
   if (g.act == ACT_I8 && g.bbits == 4) return launch_layout<A_I8_TMEM, 4, 256, 1, 3, 2>(g, stream);
