@@ -334,6 +334,22 @@ def gemm_f16xq_acc(x: np.ndarray, w_codes: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # The whole quantised linear of one configuration
 # ---------------------------------------------------------------------------
+def quantized_linear(x: np.ndarray, w_codes: np.ndarray, w_scale: np.ndarray, act: str = "none"):
+    """Quantised linear with fp16 activations and pre-quantised weights.
+
+    The chain of [BMINF 實現代碼分析2] for one decode step: ``quantize`` the
+    activations per row to int8 (``quantize_sym`` with D = 127, fp32
+    division), ``igemm`` with int32 accumulation against the weight codes
+    (8-, 4- or 2-bit values, unpacked, (N, K)), then
+    ``elementwise_copy_scale`` with the weight scale per output column and the
+    activation scale per row (``dequant``, reading Q10), and the optional
+    activation (reading Q15).  Returns (Y fp16 (M, N), x_scale fp16 (M,)).
+    """
+    xq, sx = quantize_sym(np.asarray(x), 8, "f32div")
+    c = gemm_int(xq, w_codes)
+    return dequant(c, w_scale, sx, act), sx
+
+
 def quantized_linear_i8(x: np.ndarray, w: np.ndarray):
     """Quantise activations X (M, K) and weights W (N, K) per row to int8,
     multiply in int32 and dequantise with both scales, in the order of

@@ -317,6 +317,76 @@ def test_quantized_linear_small():
     assert np.abs(y.astype(np.float64) - ref).max() < 0.05 * np.abs(ref).max()
 
 
+def test_quantized_linear_hand_example():
+    g = load("quantized_linear_hand_example.txt")
+    x = np.array([[float(v) for v in g["x"].split()]], np.float16)
+    wq = np.array([[int(v) for v in row.split()] for row in g["w_codes"].split(";")], np.int8)
+    sw = np.array([float(v) for v in g["w_scale"].split()], np.float16)
+    y, sx = O.quantized_linear(x, wq, sw)
+    assert float(sx[0]) == float(g["x_scale"])
+    assert [float(v) for v in y[0]] == [float(v) for v in g["y"].split()]
+    y_relu, _ = O.quantized_linear(x, wq, sw, "relu")
+    assert [float(v) for v in y_relu[0]] == [float(v) for v in g["y_relu"].split()]
+
+
+def brute_quantized_linear(x, wq, sw, act="none"):
+    """Pure-Python chain: per-row quantisation with struct rounding, integer
+    sums, then the fp32 products in the order int32 * w_scale * x_scale."""
+    out, scales = [], []
+    for row in x:
+        q, s = brute_quantize_row([float(v) for v in row], 8)
+        scales.append(s)
+        yrow = []
+        for j in range(wq.shape[0]):
+            c = sum(int(a) * int(b) for a, b in zip(q, wq[j]))
+            v = f32(f32(f32(float(c)) * float(sw[j])) * s)
+            if act == "relu":
+                v = max(v, 0.0)
+            yrow.append(f16(v))
+        out.append(yrow)
+    return out, scales
+
+
+@pytest.mark.parametrize("bits", [8, 4, 2])
+@pytest.mark.parametrize("act", ["none", "relu"])
+def test_quantized_linear_brute_force(bits, act):
+    rng = np.random.default_rng(14 + bits)
+    x = W.normal_f16(rng, (4, 96), 1.0)
+    x[2] *= np.float16(1e-3)                          # a row with a small scale
+    x[3] = 0                                          # a zero row: scale 0, codes 0
+    d = {8: 127, 4: 7, 2: 1}[bits]
+    wq = rng.integers(-d - (bits != 2), d + 1, size=(6, 96)).astype(np.int8)
+    sw = W.uniform_f16(rng, (6,), 1e-3, 1e-2)
+    y, sx = O.quantized_linear(x, wq, sw, act)
+    ref, ref_s = brute_quantized_linear(x, wq, sw, act)
+    assert [float(v) for v in sx] == ref_s
+    assert y.astype(np.float64).tolist() == ref
+
+
+def test_quantized_linear_lossless_activations():
+    # rows that are exactly integer codes times a power of two, absmax 127 x 2**-e:
+    # the scale is 2**-e exactly, the codes are the integers, and the result is
+    # the float64 product of X itself with the weights, rounded twice (fp32, fp16)
+    rng = np.random.default_rng(15)
+    m, n, k = 5, 7, 128
+    exps = [3, 6, 8, 10, 12]
+    q = rng.integers(-127, 128, size=(m, k))
+    q[:, 5] = 127
+    x = np.array([q[i] * 2.0 ** -exps[i] for i in range(m)], np.float16)
+    wq = rng.integers(-128, 128, size=(n, k)).astype(np.int8)
+    sw = W.uniform_f16(rng, (n,), 1e-3, 1e-2)
+    y, sx = O.quantized_linear(x, wq, sw)
+    assert [float(v) for v in sx] == [2.0 ** -e for e in exps]
+    exact = x.astype(np.float64) @ wq.astype(np.float64).T        # = C * 2**-e, exact in float64
+    for i in range(m):
+        for j in range(n):
+            c = exact[i, j] * 2.0 ** exps[i]
+            assert c == int(c)
+            assert float(y[i, j]) == f16(f32(f32(c) * float(sw[j])) * 2.0 ** -exps[i])
+            ulp = 2.0 ** (math.floor(math.log2(abs(float(y[i, j])))) - 10) if y[i, j] != 0 else 2.0 ** -24
+            assert abs(float(y[i, j]) - exact[i, j] * float(sw[j])) <= ulp
+
+
 # --------------------------------------------------------------------------
 # Roofline accounting helper
 # --------------------------------------------------------------------------
