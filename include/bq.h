@@ -252,6 +252,48 @@ bq_status bq_gemm_f16xi4_batched(const uint16_t* X, int64_t stride_x, const uint
                                  int64_t stride_y, void* stream);
 
 /*
+ * bq_quantized_linear -- the quantised linear layer with fp16 activations:
+ * per-row int8 quantisation of X, the integer GEMM against pre-quantised
+ * weights and the two-scale dequantisation, with no int8 copy of X in memory.
+ *   [BMINF 實現代碼分析2: one decode step runs quantize(h) -> igemm ->
+ *   elementwise_copy_scale; Pallas 小结与实践路线: fusing the input's
+ *   preprocessing into the matrix-multiply kernel]
+ *
+ *   x_scale[i] = fp16_rne( max_k |X[i, k]| / 127 )
+ *   q[i, k]    = the bq_quantize_sym codes (bits 8, BQ_ROUND_F32DIV) of X
+ *   Y[i, j]    = fp16_rne( act( fp32( fp32( float(Cint[i, j]) * float(w_scale[j]) )
+ *                                      * float(x_scale[i]) ) ) )
+ *   Cint[i, j] = sum_k q[i, k] * W[j, k]   (exact)
+ *   So x_scale equals bq_quantize_sym's scale and Y equals bq_gemm_*_act on
+ *   its codes with row_scale = x_scale and col_scale = w_scale, bit for bit.
+ *
+ *   X        device fp16, M x K, contiguous rows (read twice: a pass for the
+ *            row scales, then by the GEMM, which quantises each tile of X as
+ *            it converts it for the tensor cores)
+ *   W        device weights (N, K): int8 codes (bits 8) or packed 4- / 2-bit
+ *            codes in `layout` (bq_pack_weights), N * K * bits / 8 bytes
+ *   w_scale  device fp16, N (per output column)
+ *   x_scale  device fp16, M: OUTPUT, the activation scales
+ *   Y        device fp16, M x N: OUTPUT
+ *   activation  a bq_activation, as in the "_act" calls
+ *   M == 0 is an empty call.  N == 0 still writes x_scale; K == 0 writes
+ *   x_scale = 0 and Y = 0.
+ *   Limits: K % 64 == 0, N % 64 == 0; K <= 8192 (bits 8), 16384 (4), 65536
+ *   (2).  Runs on the tensor-core kernels for every M (CTA pairs, or K split
+ *   over a cluster for grids smaller than the GPU).  int8 weights with
+ *   K > 4096 need every fp32 chain to stay exact: K split 8 ways into ranges
+ *   of at most 1024 (grids of at most 18 tiles of 128 x 256) or CTA pairs
+ *   with chunked accumulation (grids that fill the GPU); the shapes between
+ *   return UNSUPPORTED.
+ *   Errors: INVALID_ARG (null pointers where data is needed, negative sizes,
+ *   bits not 8/4/2, bad layout or activation), ALIGNMENT (any pointer not
+ *   16-byte aligned), UNSUPPORTED, CUDA.
+ */
+bq_status bq_quantized_linear(const uint16_t* X, int64_t M, int64_t K, const void* W, int bits, int layout,
+                              int64_t N, const uint16_t* w_scale, int activation, uint16_t* x_scale,
+                              uint16_t* Y, void* stream);
+
+/*
  * Device-side wait status.  Every wait inside the tensor-core kernels and the
  * skinny kernel (on a shared-memory mbarrier) is bounded in time.  A wait that gives up records
  * BQ_ERR_TIMEOUT in a device status word, abandons the tile, waits (again

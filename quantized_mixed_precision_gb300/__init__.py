@@ -54,6 +54,8 @@ _SIGNATURES = {
                                              _vp, _c_i64, _vp, _c_i64, ctypes.c_int, _vp, _c_i64, _vp]),
     "bq_gemm_f16xi4_batched": (ctypes.c_int, [_vp, _c_i64, _vp, _c_i64, ctypes.c_int, _c_i64, _c_i64, _c_i64, _c_i64,
                                               _vp, _c_i64, ctypes.c_int, _vp, _c_i64, _vp]),
+    "bq_quantized_linear": (ctypes.c_int, [_vp, _c_i64, _c_i64, _vp, ctypes.c_int, ctypes.c_int, _c_i64, _vp,
+                                           ctypes.c_int, _vp, _vp, _vp]),
     "bq_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "bq_set_wait_timeout_ns": (_c_i64, [_c_i64]),
 }
@@ -377,6 +379,32 @@ def bq_gemm_i8xi2_batched(A, Bp, layout=LAYOUT_INTERLEAVED, row_scale=None, col_
 def bq_gemm_f16xi4_batched(X, Wp, col_scale, layout=LAYOUT_INTERLEAVED, activation="none", out=None, stream=None):
     return _batched("bq_gemm_f16xi4_batched", X, Wp, 4, layout, None, col_scale, activation, out, stream,
                     _torch().float16)
+
+
+def bq_quantized_linear(X, W, bits, w_scale, layout=LAYOUT_INTERLEAVED, activation="none", out=None,
+                        x_scale=None, stream=None):
+    """Fused quantised linear: X fp16 (M, K) quantised per row to int8 inside the
+    GEMM against weights W (N, K) (int8 codes, or packed 4- / 2-bit codes in
+    ``layout``) with per-column fp16 ``w_scale``.  Returns (Y fp16 (M, N),
+    x_scale fp16 (M,))."""
+    torch = _torch()
+    _need(X, torch.float16, "X", 2)
+    _need(W, torch.int8 if bits == 8 else torch.uint8, "W", 2)
+    _need(w_scale, torch.float16, "w_scale", 1)
+    M, K = X.shape
+    N = W.shape[0]
+    if W.shape[1] * 8 != K * bits:
+        raise ValueError("weight width does not match K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    if x_scale is None:
+        x_scale = torch.empty((M,), dtype=torch.float16, device=X.device)
+    _need(out, torch.float16, "out", 2)
+    _need(x_scale, torch.float16, "x_scale", 1)
+    st = lib().bq_quantized_linear(_ptr(X), M, K, _ptr(W), int(bits), _layout(layout), N, _ptr(w_scale),
+                                   _activation(activation), _ptr(x_scale), _ptr(out), _stream(stream))
+    _check(st, "bq_quantized_linear")
+    return out, x_scale
 
 
 def bq_device_status(reset=True) -> int:

@@ -62,7 +62,10 @@ bq_status run_gemm(GemmArgs g, void* stream) {
     return from_cuda(cudaMemsetAsync(g.c, 0, bytes, s));
   }
   cudaError_t e;
-  if (g.act == ACT_I8 && g.bbits == 8) {
+  if (g.act == ACT_Q8) {
+    // fp16 activations quantised inside the GEMM: the tensor-core kernels only
+    e = launch_gemm_tc(g, s);
+  } else if (g.act == ACT_I8 && g.bbits == 8) {
     // skinny M, and shapes with no exact tensor-core configuration, use dp4a
     const bool tc_ok = g.M > SKINNY_M && gemm_tc_i8_exact(g);
     e = tc_ok ? launch_gemm_tc(g, s) : launch_gemm_dp4a(g, s);
@@ -292,6 +295,30 @@ bq_status bq_gemm_f16xi4_batched(const uint16_t* X, int64_t stride_x, const uint
   GemmArgs g{X, Wp, ACT_F16, 4, layout, M, N, K, nullptr, col_scale, EPI_F16_COL, Y, activation};
   return run_batched(g, batch, stride_bytes(stride_x, 2), stride_bytes(stride_w, 1), 0, stride_bytes(stride_cs, 2),
                      stride_bytes(stride_y, 2), MAX_K, stream);
+}
+
+bq_status bq_quantized_linear(const uint16_t* X, int64_t M, int64_t K, const void* W, int bits, int layout,
+                              int64_t N, const uint16_t* w_scale, int activation, uint16_t* x_scale,
+                              uint16_t* Y, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return BQ_ERR_INVALID_ARG;
+  if (!valid_bits(bits) || !valid_layout(layout)) return BQ_ERR_INVALID_ARG;
+  if (activation != BQ_ACT_NONE && activation != BQ_ACT_RELU && activation != BQ_ACT_GELU)
+    return BQ_ERR_INVALID_ARG;
+  if (M == 0) return BQ_OK;
+  if (!x_scale || (K > 0 && !X)) return BQ_ERR_INVALID_ARG;
+  if (N > 0 && (!Y || !w_scale || (K > 0 && !W))) return BQ_ERR_INVALID_ARG;
+  const int64_t max_k = bits == 8 ? 8192 : (bits == 4 ? 16384 : MAX_K);
+  if (K % 64 != 0 || N % 64 != 0 || K > max_k || M > MAX_DIM || N > MAX_DIM) return BQ_ERR_UNSUPPORTED;
+  if (!aligned16(x_scale) || (K > 0 && !aligned16(X))) return BQ_ERR_ALIGNMENT;
+  if (N > 0 && (!aligned16(Y) || !aligned16(w_scale) || (K > 0 && !aligned16(W)))) return BQ_ERR_ALIGNMENT;
+  GemmArgs g{X, W, ACT_Q8, bits, layout, M, N, K, x_scale, w_scale, EPI_F16_ROWCOL, Y, activation};
+  // int8 weights: every fp32 chain must stay exact (decided before any launch)
+  if (bits == 8 && N > 0 && K > 0 && !gemm_tc_i8_exact(g)) return BQ_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = launch_row_scale_f16(X, M, K, x_scale, s);
+  if (e != cudaSuccess) return BQ_ERR_CUDA;
+  if (N == 0) return BQ_OK;
+  return run_gemm(g, stream);
 }
 
 bq_status bq_device_status(int* status_out, int reset) {

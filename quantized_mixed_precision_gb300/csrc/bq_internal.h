@@ -20,6 +20,10 @@ cudaError_t read_device_status(int* status_out, bool reset);
 cudaError_t launch_quantize(const void* x, int xtype, int64_t rows, int64_t cols, int64_t ld_x, int bits,
                             int mode, int8_t* q, uint16_t* scale, cudaStream_t stream);
 
+// Per-row int8 scales (D = 127) of an fp16 matrix with contiguous rows of
+// `cols` elements (cols % 8 == 0): the scales bq_quantize_sym would store.
+cudaError_t launch_row_scale_f16(const void* x, int64_t rows, int64_t cols, uint16_t* scale, cudaStream_t stream);
+
 cudaError_t launch_pack(const int8_t* q, int64_t n, int64_t k, int bits, int layout, uint8_t* packed,
                         cudaStream_t stream);
 
@@ -29,8 +33,10 @@ constexpr int BQ_DIAG_RANGE = 64;
 
 // Epilogue kinds shared by the GEMM kernels.
 enum EpiKind : int { EPI_I32 = 0, EPI_F16_COL = 1, EPI_F16_ROWCOL = 2 };
-// Activation operand kinds.
-enum ActKind : int { ACT_I8 = 0, ACT_F16 = 1 };
+// Activation operand kinds: int8 codes; fp16 values multiplied as fp16; fp16
+// values quantised per row to int8 codes inside the GEMM (with the row scales
+// passed as row_scale, already computed).
+enum ActKind : int { ACT_I8 = 0, ACT_F16 = 1, ACT_Q8 = 2 };
 
 struct GemmArgs {
   const void* a;          // activations (M, K): int8 or fp16

@@ -22,7 +22,23 @@ int sm_count();
 // k-blocks (1 when the grid fills the GPU).
 int choose_split(long long tiles, int nkb);
 
+// Swizzle mode of a raw TMA box whose rows are box_x bytes (128, 64 or 32).
+inline CUtensorMapSwizzle raw_swizzle(int box_x) {
+  return box_x == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : (box_x == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
 namespace {
+
+// Position of 16-byte chunk `chunk` of row r inside a raw box with rows of
+// BOX_X bytes, as the box's swizzle placed it (bits 4.. of the address XOR
+// bits 7..: 128B swizzle 3 bits, 64B 2 bits, 32B 1 bit).
+template <int BOX_X>
+__device__ __forceinline__ int raw_chunk_pos(int chunk, int r) {
+  static_assert(BOX_X == 128 || BOX_X == 64 || BOX_X == 32, "raw box row width");
+  if constexpr (BOX_X == 128) return chunk ^ (r & 7);
+  else if constexpr (BOX_X == 64) return chunk ^ ((r >> 1) & 3);
+  else return chunk ^ ((r >> 2) & 1);
+}
 
 // Store one 16-byte fp16 chunk (logical chunk lc = 8 k values) of row r into a
 // 128B-swizzled K-major tile (chunk c of row r lives at position c ^ (r & 7)).

@@ -19,9 +19,10 @@
 // Warp roles per CTA.  The converters come in groups that take the k-blocks
 // in turn (group g of n converts kb = g mod n), so the fixed cost of each
 // k-block's waits and arrivals overlaps across groups:
-//   P_NA groups of 4 warps    A: int8 activation row (thread = row = TMEM
+//   NA groups of 4 warps      A: int8 activation row (thread = row = TMEM
 //                             lane) -> 32 fp16 pairs -> tcgen05.st into a
-//                             TMEM stage.
+//                             TMEM stage (AQ: fp16 activation row ->
+//                             int8 codes as fp16 pairs, the same way).
 //   NB groups of P_BW warps   B: raw weight codes -> fp16 128B-swizzled
 //                             K-major tile in shared memory.
 //   next warp                 allocates tensor memory (collectively with the
@@ -62,6 +63,7 @@
 #include "bq_device.cuh"
 #include "bq_internal.h"
 #include "gemm_common.cuh"
+#include "quant_math.cuh"
 
 namespace bq {
 namespace {
@@ -69,10 +71,11 @@ namespace {
 constexpr int PM = 128;                  // tile rows per CTA (256 per pair)
 constexpr int PK = 64;                   // k per block: one 128-byte fp16 swizzle row
 constexpr int P_NA = 2;                  // activation converter groups (4 warps each)
+constexpr int P_NA_Q = 4;                // the same, quantising fp16 activations
+constexpr int P_NB_Q = 4;                // weight converter groups beside them
 constexpr int P_NB_I8 = 6;               // weight converter groups, int8 activations
 constexpr int P_NB_F16 = 6;              // weight converter groups, fp16 activations
 constexpr int P_BW = 2;                  // warps per weight converter group
-constexpr int P_A_WARPS = 4 * P_NA;
 constexpr int P_B_THREADS = P_BW * 32;   // weight converters per group
 constexpr uint64_t P_DRAIN_NS = 4000000000ull;
 constexpr int CH_KB = 15;                // k-blocks per accumulation chunk (DR mode)
@@ -81,19 +84,25 @@ constexpr float H_UNIT = 8192.0f;        // weight of one high-part unit (2**13)
 // AF16: fp16 activations, loaded by TMA straight into the MMA's 128B-swizzled
 // K-major layout (no activation converters, A read from shared memory), and
 // two accumulator slices of half of K each (shorter fp32 chains).  Otherwise
-// int8 activations, converted into tensor memory, one accumulator.
-template <int BBITS, int BN, int ST, int RST, bool AF16>
+// int8 activations, converted into tensor memory, one accumulator; with AQ
+// the activations arrive as fp16 and the activation converters quantise them
+// to int8 codes (the row scales given) before storing them the same way.
+template <int BBITS, int BN, int ST, int RST, bool AF16, bool AQ = false>
 struct PairCfg {
   static constexpr int HB = BN / 2;                            // weight rows per CTA
-  static constexpr int A_WARPS = AF16 ? 0 : P_A_WARPS;
-  static constexpr int NA = AF16 ? 0 : P_NA;                   // activation converter groups
-  static constexpr int NB = AF16 ? P_NB_F16 : P_NB_I8;        // weight converter groups
+  // quantising converters (AQ) do several times the work of an int8 conversion: more of them
+  static constexpr int NA = AF16 ? 0 : (AQ ? P_NA_Q : P_NA);  // activation converter groups
+  static constexpr int A_WARPS = 4 * NA;
+  static constexpr int NB = AF16 ? P_NB_F16 : (AQ ? P_NB_Q : P_NB_I8);   // weight converter groups
   static constexpr int CONSUMER_WARPS = A_WARPS + NB * P_BW;
   static constexpr int MMA_WARP = CONSUMER_WARPS;
   static constexpr int PRODUCER_WARP = MMA_WARP + 1;
   static constexpr int THREADS = (PRODUCER_WARP + 1) * 32;
-  // a raw stage holds RKB k-blocks so that every TMA box row is 128 bytes (64 for 2-bit weights)
-  static constexpr int RKB = BBITS == 8 ? 2 : 4;
+  // a raw stage holds RKB k-blocks so that every TMA box row is 128 bytes (64
+  // for 2-bit weights); fp16 activations to quantise fill 128-byte rows with
+  // one k-block, and keep raw stages of 2 k-blocks (weight rows of 64 or 32
+  // bytes for 4- and 2-bit weights)
+  static constexpr int RKB = (BBITS == 8 || AQ) ? 2 : 4;
   static constexpr int B_RAW_ROW = PK * BBITS / 8;             // raw weight bytes per row per k-block
   static constexpr int B_BOX_X = RKB * B_RAW_ROW;
   static constexpr int B_PIECES_ROW = B_RAW_ROW / 16;          // 16-byte pieces per row per k-block
@@ -101,11 +110,12 @@ struct PairCfg {
   static constexpr int NPB = (B_PIECES + P_B_THREADS - 1) / P_B_THREADS;
   static constexpr int B_RAW = HB * B_BOX_X;
   static constexpr int A_BOX = PM * 128;                       // int8 activations: 2 k-blocks x 128 rows
-  static constexpr int A_RAW = AF16 ? 0 : A_BOX * (RKB / 2);
+  static constexpr int A_KB = PM * 128;                        // fp16 activations: 1 k-block x 128 rows
+  static constexpr int A_RAW = AF16 ? 0 : (AQ ? A_KB * RKB : A_BOX * (RKB / 2));
   static constexpr int A_TILE = AF16 ? PM * 128 : 0;           // fp16 activation tile of one MMA stage
   static constexpr int B_TILE = HB * 128;                      // fp16 weight tile of one MMA stage
   static constexpr int STAGE = A_TILE + B_TILE;
-  static constexpr int RSTAGE = A_RAW + B_RAW;
+  static constexpr int RSTAGE = (A_RAW + B_RAW + 1023) / 1024 * 1024;
   static constexpr int NACC = AF16 ? 2 : 1;                    // accumulator slices
   static constexpr int A_COLS = PK / 2;                        // TMEM columns of one activation stage
   static constexpr int ACC_COLS = NACC * BN;
@@ -128,10 +138,11 @@ struct PairCfg {
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "pair MMA N and 32-column epilogue chunks");
   static_assert(CONSUMER_WARPS % 4 == 0 && THREADS <= 1024, "warp roles");
   static_assert(!AF16 || BBITS == 4, "fp16 activations pair with 4-bit weights");
+  static_assert(!(AF16 && AQ), "one activation form");
   // A group that has finished k-block kb - n (n groups) knows that the MMAs of
   // kb - n - ST are done; its wait for the stage of kb must not pass on the
   // parity of a phase two behind, which needs n <= ST.
-  static_assert(P_NA <= ST && NB <= ST, "converter groups per stage ring");
+  static_assert(NA <= ST && NB <= ST, "converter groups per stage ring");
   static_assert(CONSUMER_WARPS * STG_BYTES <= OFF_BAR, "epilogue staging fits in the pipeline buffers");
   static_assert((3 * ST + 2 * RST + 3) * 8 + 4 <= 256, "barrier area");
 };
@@ -231,13 +242,13 @@ __device__ __forceinline__ bool pair_drain(int b, uint32_t tmem, uint64_t* chunk
 // separate instantiation, so the kernel without one carries no trace of it).
 // DR: chunked accumulation (int8 x int8, K > 1024); `out` is the output
 // (also the home of the running high parts), used only in that mode.
-template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool ACTV, bool DR>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST, AF16>::THREADS, 1)
+template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool AQ, bool ACTV, bool DR>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST, AF16, AQ>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, int M, int N, int K,
                      const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
                      void* out, uint64_t timeout_ns, int* status) {
-  using C = PairCfg<BBITS, BN, ST, RST, AF16>;
+  using C = PairCfg<BBITS, BN, ST, RST, AF16, AQ>;
   static_assert(!DR || (BBITS == 8 && !AF16), "chunked accumulation is for int8 x int8");
   // DR: each consumer warp drains at most two 32-column chunks of its quadrant
   static_assert(!DR || BN / 32 <= 2 * (C::CONSUMER_WARPS / 4), "drain chunks per warp");
@@ -325,7 +336,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
           if (!mbar_wait(&rempty_bar[rs], ((grp / RST) & 1) ^ 1, timeout_ns, status)) break;
           uint8_t* raw = smem + C::OFF_RAW + rs * C::RSTAGE;
           mbar_arrive_expect_tx(&rfull_bar[rs], C::A_RAW + C::B_RAW);
-          if constexpr (!AF16) {
+          if constexpr (AQ) {
+#pragma unroll
+            for (int b = 0; b < C::RKB; ++b)
+              tma_load_2d(raw + b * C::A_KB, &tmap_a, (kb + b) * PK, m0, &rfull_bar[rs]);
+          } else if constexpr (!AF16) {
 #pragma unroll
             for (int b = 0; b < C::RKB / 2; ++b)
               tma_load_2d(raw + b * C::A_BOX, &tmap_a, (kb + 2 * b) * PK, m0, &rfull_bar[rs]);
@@ -398,35 +413,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
     __syncwarp();
   } else if (warp < C::A_WARPS) {
     // ------------------------------------------------------------ int8 activations -> TMEM
-    // A group g (warps 4g .. 4g + 3) converts the k-blocks kb = g (mod P_NA)
+    // A group g (warps 4g .. 4g + 3) converts the k-blocks kb = g (mod NA)
     const int q = warp & 3;                               // TMEM lane quadrant
     const int r = q * 32 + lane;                          // tile row == TMEM lane
-    for (int kb = warp >> 2; kb < nkb; kb += P_NA) {
+    RowQuant rq{};
+    if constexpr (AQ) rq = row_quant(m0 + r < M ? __half2float(row_scale[m0 + r]) : 0.0f);
+    for (int kb = warp >> 2; kb < nkb; kb += C::NA) {
       if (!drain_before(kb)) {
         ok = false;
         break;
       }
       const int grp = kb / C::RKB, rs = grp % RST;
       // the group's first k-block of a raw stage waits for it to land
-      if (kb % C::RKB < P_NA && !warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
+      if (kb % C::RKB < C::NA && !warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
         ok = false;
         break;
       }
-      // this k-block is half of a 128-byte box row (128B swizzle: chunk c of row r at c ^ (r & 7))
-      const uint8_t* box = smem + C::OFF_RAW + rs * C::RSTAGE + ((kb % C::RKB) >> 1) * C::A_BOX + r * 128;
-      const int c0 = (kb & 1) * 4;
-      uint4 v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(box + (((c0 + j) ^ (r & 7)) << 4));
-      if ((kb % C::RKB) + P_NA >= C::RKB || kb + P_NA >= nkb)   // group's last use
-        mbar_arrive_after_loads(&rempty_bar[rs], fold4(v[0]) ^ fold4(v[1]) ^ fold4(v[2]) ^ fold4(v[3]), rzero);
+      const bool last_use = (kb % C::RKB) + C::NA >= C::RKB || kb + C::NA >= nkb;   // the group's last use
       uint32_t h[32];
+      if constexpr (AQ) {
+        // this k-block is one 128-byte box row of fp16 values (chunk c of row r at c ^ (r & 7))
+        const uint8_t* box = smem + C::OFF_RAW + rs * C::RSTAGE + (kb % C::RKB) * C::A_KB + r * 128;
+        quant64_f16_codes(box, r, rq, h);
+        // the codes depend on every value read, so the release follows those reads
+        if (last_use) {
+          uint32_t dep = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        cvt_i8x4_f16(v[j].x, h[8 * j + 0], h[8 * j + 1]);
-        cvt_i8x4_f16(v[j].y, h[8 * j + 2], h[8 * j + 3]);
-        cvt_i8x4_f16(v[j].z, h[8 * j + 4], h[8 * j + 5]);
-        cvt_i8x4_f16(v[j].w, h[8 * j + 6], h[8 * j + 7]);
+          for (int i = 0; i < 32; ++i) dep ^= h[i];
+          mbar_arrive_after_loads(&rempty_bar[rs], dep, rzero);
+        }
+      } else {
+        // this k-block is half of a 128-byte box row (128B swizzle: chunk c of row r at c ^ (r & 7))
+        const uint8_t* box = smem + C::OFF_RAW + rs * C::RSTAGE + ((kb % C::RKB) >> 1) * C::A_BOX + r * 128;
+        const int c0 = (kb & 1) * 4;
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(box + (((c0 + j) ^ (r & 7)) << 4));
+        if (last_use)
+          mbar_arrive_after_loads(&rempty_bar[rs], fold4(v[0]) ^ fold4(v[1]) ^ fold4(v[2]) ^ fold4(v[3]), rzero);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          cvt_i8x4_f16(v[j].x, h[8 * j + 0], h[8 * j + 1]);
+          cvt_i8x4_f16(v[j].y, h[8 * j + 2], h[8 * j + 3]);
+          cvt_i8x4_f16(v[j].z, h[8 * j + 4], h[8 * j + 5]);
+          cvt_i8x4_f16(v[j].w, h[8 * j + 6], h[8 * j + 7]);
+        }
       }
       const int s = kb % ST;
       if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) {
@@ -466,7 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         const int pi = c + i * P_B_THREADS;
         const int r = pi % C::HB, sub = pi / C::HB;
         const int chunk = (kb % C::RKB) * C::B_PIECES_ROW + sub;
-        const int pos = C::B_BOX_X == 128 ? (chunk ^ (r & 7)) : (chunk ^ ((r >> 1) & 3));
+        const int pos = raw_chunk_pos<C::B_BOX_X>(chunk, r);
         v[i] = pi < C::B_PIECES ? *reinterpret_cast<const uint4*>(raw + r * C::B_BOX_X + (pos << 4))
                                 : make_uint4(0, 0, 0, 0);
       }
@@ -632,20 +663,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool ACTV, bool DR>
+template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool AQ, bool ACTV, bool DR>
 cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
-  using C = PairCfg<BBITS, BN, ST, RST, AF16>;
+  using C = PairCfg<BBITS, BN, ST, RST, AF16, AQ>;
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
   CUtensorMap ma, mb, mc;
-  if (AF16)   // one k-block of fp16 rows: 128 bytes, the MMA's 128B swizzle
+  if (AF16 || AQ)   // one k-block of fp16 rows: 128 bytes, the MMA's (or the converters') 128B swizzle
     e = make_map(&ma, g.a, 2, (uint64_t)g.K, (uint64_t)g.M, PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
   else        // two k-blocks of int8 rows
     e = make_map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, 2 * PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_BOX_X, C::HB,
-               C::B_BOX_X == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+  e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_BOX_X, C::HB, raw_swizzle(C::B_BOX_X));
   if (e != cudaSuccess) return e;
   // output boxes of 32 x 32: int32 rows of 128 bytes, fp16 rows of 64 bytes
   if (g.epi == EPI_I32)
@@ -653,7 +683,7 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   else
     e = make_map(&mc, g.c, 2, (uint64_t)g.N, (uint64_t)g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, AF16, ACTV, DR>;
+  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, AF16, AQ, ACTV, DR>;
   e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(2 * ((g.M + 2 * PM - 1) / (2 * PM))), (unsigned)((g.N + BN - 1) / BN));
@@ -664,23 +694,23 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int BBITS, int BN, int ST, int RST, bool AF16, bool ACTV>
+template <int BBITS, int BN, int ST, int RST, bool AF16, bool AQ, bool ACTV>
 cudaError_t launch_pair_act(const GemmArgs& g, cudaStream_t stream) {
   if constexpr (BBITS == 8 && !AF16) {
     // int8 x int8 beyond 16 k-blocks: chunked accumulation keeps the sums exact
-    if (g.K > 16 * PK) return launch_pair_t<8, BN, true, ST, RST, false, ACTV, true>(g, stream);
-    return launch_pair_t<8, BN, true, ST, RST, false, ACTV, false>(g, stream);
+    if (g.K > 16 * PK) return launch_pair_t<8, BN, true, ST, RST, false, AQ, ACTV, true>(g, stream);
+    return launch_pair_t<8, BN, true, ST, RST, false, AQ, ACTV, false>(g, stream);
   } else {
     if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN)
-      return launch_pair_t<BBITS, BN, false, ST, RST, AF16, ACTV, false>(g, stream);
-    return launch_pair_t<BBITS, BN, true, ST, RST, AF16, ACTV, false>(g, stream);
+      return launch_pair_t<BBITS, BN, false, ST, RST, AF16, AQ, ACTV, false>(g, stream);
+    return launch_pair_t<BBITS, BN, true, ST, RST, AF16, AQ, ACTV, false>(g, stream);
   }
 }
 
-template <int BBITS, int BN, int ST, int RST, bool AF16 = false>
+template <int BBITS, int BN, int ST, int RST, bool AF16 = false, bool AQ = false>
 cudaError_t launch_pair_layout(const GemmArgs& g, cudaStream_t stream) {
-  if (g.actfn != BQ_ACT_NONE) return launch_pair_act<BBITS, BN, ST, RST, AF16, true>(g, stream);
-  return launch_pair_act<BBITS, BN, ST, RST, AF16, false>(g, stream);
+  if (g.actfn != BQ_ACT_NONE) return launch_pair_act<BBITS, BN, ST, RST, AF16, AQ, true>(g, stream);
+  return launch_pair_act<BBITS, BN, ST, RST, AF16, AQ, false>(g, stream);
 }
 
 cudaError_t launch_pair_f16(const GemmArgs& g, int bn, cudaStream_t stream) {
@@ -689,6 +719,19 @@ cudaError_t launch_pair_f16(const GemmArgs& g, int bn, cudaStream_t stream) {
     case 224: return launch_pair_layout<4, 224, 6, 3, true>(g, stream);
     case 192: return launch_pair_layout<4, 192, 6, 3, true>(g, stream);
     case 160: return launch_pair_layout<4, 160, 6, 3, true>(g, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// fp16 activations quantised in the converters: raw stages of 2 k-blocks
+// with twice the activation bytes, so fewer of them fit
+template <int BBITS>
+cudaError_t launch_pair_q(const GemmArgs& g, int bn, cudaStream_t stream) {
+  switch (bn) {
+    case 256: return launch_pair_layout<BBITS, 256, 6, BBITS == 8 ? 2 : 3, false, true>(g, stream);
+    case 224: return launch_pair_layout<BBITS, 224, 6, 3, false, true>(g, stream);
+    case 192: return launch_pair_layout<BBITS, 192, 6, 3, false, true>(g, stream);
+    case 160: return launch_pair_layout<BBITS, 160, 6, 3, false, true>(g, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -737,6 +780,12 @@ int gemm_pair_bn(const GemmArgs& g) {
 
 cudaError_t launch_gemm_pair(const GemmArgs& g, int bn, cudaStream_t stream) {
   if (g.act == ACT_F16) return launch_pair_f16(g, bn, stream);
+  if (g.act == ACT_Q8) {
+    if (g.bbits == 4) return launch_pair_q<4>(g, bn, stream);
+    if (g.bbits == 2) return launch_pair_q<2>(g, bn, stream);
+    if (g.bbits == 8) return launch_pair_q<8>(g, bn, stream);
+    return cudaErrorInvalidValue;
+  }
   if (g.bbits == 4) return launch_pair_bits<4>(g, bn, stream);
   if (g.bbits == 2) return launch_pair_bits<2>(g, bn, stream);
   if (g.bbits == 8) return launch_pair_bits<8>(g, bn, stream);

@@ -46,6 +46,7 @@
 #include "bq_device.cuh"
 #include "bq_internal.h"
 #include "gemm_common.cuh"
+#include "quant_math.cuh"
 
 namespace bq {
 
@@ -147,7 +148,11 @@ constexpr int BK = 64;                 // k per block: one 128-byte fp16 swizzle
 constexpr int B_THREADS = 256;         // one weight-converter group (8 warps) per k-block
 constexpr uint64_t DRAIN_TIMEOUT_NS = 4000000000ull;
 
-enum AMode : int { A_I8_TMEM = 0, A_F16_SMEM = 1 };
+// A_I8_TMEM: int8 codes, converted into TMEM stages.  A_F16_SMEM: fp16
+// values loaded straight into the MMA's shared-memory layout.  A_Q_TMEM: fp16
+// values quantised per row to int8 codes (row scales given) by the same
+// converters, which then store the codes into TMEM stages as with A_I8_TMEM.
+enum AMode : int { A_I8_TMEM = 0, A_F16_SMEM = 1, A_Q_TMEM = 2 };
 
 // Converter groups per CTA.
 constexpr int TC_NG = 1;
@@ -156,37 +161,42 @@ constexpr int TC_NG = 1;
 // kb = g (mod NG)), so conversion of consecutive k-blocks overlaps.
 template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST, int NG, int MINB = 1>
 struct Cfg {
-  static constexpr int A_WARPS = AMODE == A_I8_TMEM ? 4 * NG : 0;
+  static constexpr bool A_TMEM = AMODE != A_F16_SMEM;          // A converted into TMEM stages
+  static constexpr int A_WARPS = A_TMEM ? 4 * NG : 0;
   static constexpr int B_WARPS = 8 * NG;
   static constexpr int MMA_WARP = A_WARPS + B_WARPS;
   static constexpr int PRODUCER_WARP = MMA_WARP + 1;
   static constexpr int THREADS = (PRODUCER_WARP + 1) * 32;
   // A raw stage holds RKB k-blocks, so every TMA box row is 128 bytes (64
   // for 2-bit weights): the TMA engine moves a box row by row, and narrow
-  // rows waste its request rate.
-  static constexpr int RKB = BBITS == 8 ? 2 : 4;
+  // rows waste its request rate.  Quantised fp16 activations take 128 bytes
+  // per row per k-block already, and keep raw stages of 2 k-blocks.
+  static constexpr int RKB = (BBITS == 8 || AMODE == A_Q_TMEM) ? 2 : 4;
   static constexpr int B_RAW_ROW = BK * BBITS / 8;            // raw weight bytes per row per k-block
-  static constexpr int B_BOX_X = RKB * B_RAW_ROW;             // bytes per raw weight box row (128 or 64)
+  static constexpr int B_BOX_X = RKB * B_RAW_ROW;             // bytes per raw weight box row (128, 64 or 32)
   static constexpr int B_PIECES_ROW = B_RAW_ROW / 16;         // 16-byte pieces per row per k-block
   static constexpr int B_PIECES = BN * B_PIECES_ROW;
   static constexpr int NPB = (B_PIECES + B_THREADS - 1) / B_THREADS;
   static constexpr int B_RAW = BN * B_BOX_X;                  // raw weight bytes per raw stage
   static constexpr int A_BOX = BM * 128;                      // one int8 A box: 2 k-blocks x 128 rows
-  static constexpr int A_RAW = AMODE == A_I8_TMEM ? A_BOX * (RKB / 2) : 0;   // int8 raw A per raw stage
+  static constexpr int A_KB = BM * 128;                       // one fp16 A box: 1 k-block x 128 rows
+  static constexpr int A_RAW = AMODE == A_I8_TMEM   ? A_BOX * (RKB / 2)          // raw A per raw stage
+                               : AMODE == A_Q_TMEM ? A_KB * RKB
+                                                   : 0;
   static constexpr int A_TILE = AMODE == A_F16_SMEM ? BM * 128 : 0; // fp16 A tile in the MMA stage
   static constexpr int B_TILE = BN * 128;
   static constexpr int STAGE = A_TILE + B_TILE;
-  static constexpr int RSTAGE = A_RAW + B_RAW;
+  static constexpr int RSTAGE = (A_RAW + B_RAW + 1023) / 1024 * 1024;
   static constexpr int A_COLS = BK / 2;                        // TMEM columns of one A stage
   static constexpr int ACC_COLS = NACC * BN;
-  static constexpr int USED_COLS = ACC_COLS + (AMODE == A_I8_TMEM ? ST * A_COLS : 0);
+  static constexpr int USED_COLS = ACC_COLS + (A_TMEM ? ST * A_COLS : 0);
   static constexpr int NCOLS = USED_COLS <= 128 ? 128 : (USED_COLS <= 256 ? 256 : 512);
   static constexpr int OFF_RAW = ST * STAGE;
   static constexpr int OFF_BAR = OFF_RAW + RST * RSTAGE;
   static constexpr size_t SMEM = (size_t)OFF_BAR + 256 + 1024;
   static_assert(USED_COLS <= 512 / MINB, "tensor memory budget (MINB CTAs per SM)");
   static_assert(MINB * (SMEM + 1024) <= 233472 && SMEM <= 232448, "shared memory budget");
-  static_assert(STAGE % 1024 == 0 && RSTAGE % 1024 == 0, "stage alignment");
+  static_assert(STAGE % 1024 == 0 && A_RAW % 1024 == 0, "stage alignment");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert((BN / (2 * NG)) % 32 == 0, "epilogue column parts are whole 32-column chunks");
 };
@@ -269,6 +279,10 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
 #pragma unroll
             for (int b = 0; b < C::RKB / 2; ++b)
               tma_load_2d(raw + b * C::A_BOX, &tmap_a, (kb_lo + kb + 2 * b) * BK, m0, &rfull_bar[rs]);
+          } else if constexpr (AMODE == A_Q_TMEM) {
+#pragma unroll
+            for (int b = 0; b < C::RKB; ++b)
+              tma_load_2d(raw + b * C::A_KB, &tmap_a, (kb_lo + kb + b) * BK, m0, &rfull_bar[rs]);
           }
           tma_load_2d(raw + C::A_RAW, &tmap_b, (kb_lo + kb) * C::B_RAW_ROW, n0, &rfull_bar[rs]);
           issued_groups = grp + 1;
@@ -336,24 +350,39 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
     // ------------------------------------------------------------ int8 A -> TMEM
     const int q = warp & 3;                               // TMEM lane quadrant
     const int r = q * 32 + lane;                          // tile row == TMEM lane
+    RowQuant rq{};
+    if constexpr (AMODE == A_Q_TMEM) rq = row_quant(m0 + r < M ? __half2float(row_scale[m0 + r]) : 0.0f);
     for (int kb = warp >> 2; kb < nkb; kb += NG) {
       const int grp = kb / C::RKB, rs = grp % RST;
       if (!warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) break;
-      // this k-block is half of a 128-byte box row (128B swizzle: chunk c of row r at c ^ (r & 7))
-      const uint8_t* box = smem + C::OFF_RAW + rs * C::RSTAGE + ((kb % C::RKB) >> 1) * C::A_BOX + r * 128;
-      const int c0 = (kb & 1) * 4;
-      uint4 v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(box + (((c0 + j) ^ (r & 7)) << 4));
-      if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb)   // group's last use
-        mbar_arrive_after_loads(&rempty_bar[rs], fold4(v[0]) ^ fold4(v[1]) ^ fold4(v[2]) ^ fold4(v[3]), rzero);
       uint32_t h[32];
+      if constexpr (AMODE == A_Q_TMEM) {
+        // this k-block is one 128-byte box row of fp16 values (chunk c of row r at c ^ (r & 7))
+        const uint8_t* box = smem + C::OFF_RAW + rs * C::RSTAGE + (kb % C::RKB) * C::A_KB + r * 128;
+        quant64_f16_codes(box, r, rq, h);
+        // the codes depend on every value read, so the release follows those reads
+        if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb) {   // group's last use
+          uint32_t dep = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        cvt_i8x4_f16(v[j].x, h[8 * j + 0], h[8 * j + 1]);
-        cvt_i8x4_f16(v[j].y, h[8 * j + 2], h[8 * j + 3]);
-        cvt_i8x4_f16(v[j].z, h[8 * j + 4], h[8 * j + 5]);
-        cvt_i8x4_f16(v[j].w, h[8 * j + 6], h[8 * j + 7]);
+          for (int i = 0; i < 32; ++i) dep ^= h[i];
+          mbar_arrive_after_loads(&rempty_bar[rs], dep, rzero);
+        }
+      } else {
+        // this k-block is half of a 128-byte box row (128B swizzle: chunk c of row r at c ^ (r & 7))
+        const uint8_t* box = smem + C::OFF_RAW + rs * C::RSTAGE + ((kb % C::RKB) >> 1) * C::A_BOX + r * 128;
+        const int c0 = (kb & 1) * 4;
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4*>(box + (((c0 + j) ^ (r & 7)) << 4));
+        if ((kb % C::RKB) + NG >= C::RKB || kb + NG >= nkb)   // group's last use
+          mbar_arrive_after_loads(&rempty_bar[rs], fold4(v[0]) ^ fold4(v[1]) ^ fold4(v[2]) ^ fold4(v[3]), rzero);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          cvt_i8x4_f16(v[j].x, h[8 * j + 0], h[8 * j + 1]);
+          cvt_i8x4_f16(v[j].y, h[8 * j + 2], h[8 * j + 3]);
+          cvt_i8x4_f16(v[j].z, h[8 * j + 4], h[8 * j + 5]);
+          cvt_i8x4_f16(v[j].w, h[8 * j + 6], h[8 * j + 7]);
+        }
       }
       const int s = kb % ST;
       if (!warp_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) break;
@@ -383,7 +412,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
         const int pi = c + i * B_THREADS;
         const int r = pi % BN, sub = pi / BN;
         const int chunk = (kb % C::RKB) * C::B_PIECES_ROW + sub;
-        const int pos = C::B_BOX_X == 128 ? (chunk ^ (r & 7)) : (chunk ^ ((r >> 1) & 3));
+        const int pos = raw_chunk_pos<C::B_BOX_X>(chunk, r);
         v[i] = pi < C::B_PIECES ? *reinterpret_cast<const uint4*>(raw + r * C::B_BOX_X + (pos << 4))
                                 : make_uint4(0, 0, 0, 0);
       }
@@ -441,7 +470,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
         }
         const int ncol = n0 + col;
         // integer operands: the dequantisation starts from the exact integer sum of the slices
-        if (AMODE == A_I8_TMEM && NACC > 1) {
+        if (C::A_TMEM && NACC > 1) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __int2float_rn(iv[i]);
         }
@@ -546,12 +575,12 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
               const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                if constexpr (AMODE == A_I8_TMEM) iacc[4 * j + e] += __float2int_rn(__uint_as_float(w[e]));
+                if constexpr (C::A_TMEM) iacc[4 * j + e] += __float2int_rn(__uint_as_float(w[e]));
                 else acc[4 * j + e] += __uint_as_float(w[e]);
               }
             }
           }
-          if constexpr (AMODE == A_I8_TMEM) {
+          if constexpr (C::A_TMEM) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = __int2float_rn(iacc[i]);
           }
@@ -561,7 +590,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
               int4* dst = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + (size_t)row * N + ncol);
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                if constexpr (AMODE == A_I8_TMEM)
+                if constexpr (C::A_TMEM)
                   dst[i] = make_int4(iacc[4 * i], iacc[4 * i + 1], iacc[4 * i + 2], iacc[4 * i + 3]);
                 else
                   dst[i] = make_int4(__float2int_rn(acc[4 * i]), __float2int_rn(acc[4 * i + 1]),
@@ -615,14 +644,13 @@ cudaError_t launch_t(const GemmArgs& g, int split, cudaStream_t stream) {
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
   CUtensorMap ma, mb;
-  if (AMODE == A_F16_SMEM) {
+  if (AMODE != A_I8_TMEM) {   // fp16 rows, one k-block per box
     e = make_map(&ma, g.a, 2, (uint64_t)g.K, (uint64_t)g.M, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     e = make_map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, 2 * BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (e != cudaSuccess) return e;
-  e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_BOX_X, BN,
-               C::B_BOX_X == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+  e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_BOX_X, BN, raw_swizzle(C::B_BOX_X));
   if (e != cudaSuccess) return e;
   auto kern = gemm_tc_kernel<AMODE, BBITS, BN, NACC, INTER, ST, RST, NG, MINB>;
   e = set_smem_once(kern, (int)C::SMEM);
@@ -688,6 +716,20 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream) {
       case 4: return launch_layout<A_I8_TMEM, 8, 64, 4, 4, 2, 1>(g, stream);
       default: return cudaErrorInvalidValue;
     }
+  }
+  if (g.act == ACT_Q8) {
+    // fp16 activations quantised in the converters: the int8 paths' chains
+    if (g.bbits == 8) {
+      switch (tc_i8_slices(g)) {
+        case 1: return launch_layout<A_Q_TMEM, 8, 256, 1, 3, 2>(g, stream);
+        case 2: return launch_layout<A_Q_TMEM, 8, 128, 2, 4, 2>(g, stream);
+        case 4: return launch_layout<A_Q_TMEM, 8, 64, 4, 4, 2, 1>(g, stream);
+        default: return cudaErrorInvalidValue;
+      }
+    }
+    if (g.bbits == 4) return launch_layout<A_Q_TMEM, 4, 256, 1, 3, 2>(g, stream);
+    if (g.bbits == 2) return launch_layout<A_Q_TMEM, 2, 256, 1, 4, 2>(g, stream);
+    return cudaErrorInvalidValue;
   }
   // int8 activations with 4- / 2-bit weights: every partial sum < 2**24 (host-bounded K)
   if (g.act == ACT_I8 && g.bbits == 4) return launch_layout<A_I8_TMEM, 4, 256, 1, 3, 2>(g, stream);

@@ -12,67 +12,13 @@
 #include "bq_device.cuh"
 #include "bq_internal.h"
 #include "gemm_common.cuh"
+#include "quant_math.cuh"
 
 namespace bq {
 
 namespace {
 
 __device__ __forceinline__ int qmax_of(int bits) { return bits == 8 ? 127 : (bits == 4 ? 7 : 1); }
-
-constexpr float RNE_MAGIC = 12582912.0f;   // 1.5 * 2**23: adding it rounds |t| < 2**22 to an integer (ties to even)
-
-// Code for one element from the stored fp16 scale s (as float) and its
-// reciprocal rcp = RN(1 / s) (0 when s == 0, which yields code 0), returned
-// as a float that carries the code in its low byte (two's complement).  In
-// F32DIV mode the code is rne(RN(x / s)) clamped to [-d, d].  RN(x * rcp)
-// differs from RN(x / s) by less than 2**-14 for |x / s| < 256, so both round
-// to the same integer unless the product lies within 2**-12 of a
-// half-integer; only then is the IEEE division evaluated.  The rounding is
-// t + 1.5 * 2**23 in fp32 (round to nearest even), whose low mantissa bits are
-// then the integer, so no float -> int conversion is needed; clamping before
-// the rounding equals clamping after it, the bounds being integers.
-__device__ __forceinline__ float code_exact(float x, float s, float fd, int mode) {
-  float t = s == 0.0f ? 0.0f : __fdiv_rn(x, s);
-  if (mode == BQ_ROUND_BMINF_HALF) t = __half2float(__float2half_rn(t));
-  return __fadd_rn(fminf(fmaxf(t, -fd), fd), RNE_MAGIC);
-}
-
-// Fast form for F32DIV: the code of x, and whether the product was too close
-// to a half-integer for it to be trusted (then code_exact decides).
-__device__ __forceinline__ float code_fast(float x, float rcp, float fd, bool& unsure) {
-  const float tc = fminf(fmaxf(__fmul_rn(x, rcp), -fd), fd);
-  const float m = __fadd_rn(tc, RNE_MAGIC);
-  unsure = fabsf(tc - __fsub_rn(m, RNE_MAGIC)) > 0.5f - 2.44140625e-4f;
-  return m;
-}
-
-__device__ __forceinline__ float quant_one(float x, float s, float rcp, float fd, int mode) {
-  if (mode == BQ_ROUND_BMINF_HALF) return code_exact(x, s, fd, mode);
-  bool unsure;
-  const float m = code_fast(x, rcp, fd, unsure);
-  return unsure ? code_exact(x, s, fd, mode) : m;
-}
-
-__device__ __forceinline__ uint32_t code_byte(float m) { return __float_as_uint(m); }
-
-// Fast F32DIV form for two elements with packed fp32x2 arithmetic (each lane
-// of a packed op is an ordinary IEEE round-to-nearest operation): the codes
-// m = RN(x * rcp) + 1.5 * 2**23 and the distances |RN(x * rcp) - rne(.)|.
-__device__ __forceinline__ void code_fast2(float x0, float x1, float rcp, float& m0, float& m1, float& d0,
-                                           float& d1) {
-  asm("{\n\t.reg .b64 x, c, g, t, m, r, d;\n\t"
-      "mov.b64 x, {%4, %5};\n\t"
-      "mov.b64 c, {%6, %6};\n\t"
-      "mov.b64 g, {%7, %7};\n\t"
-      "mul.rn.f32x2 t, x, c;\n\t"
-      "add.rn.f32x2 m, t, g;\n\t"
-      "sub.rn.f32x2 r, m, g;\n\t"
-      "sub.rn.f32x2 d, t, r;\n\t"
-      "mov.b64 {%0, %1}, m;\n\t"
-      "mov.b64 {%2, %3}, d;\n\t}"
-      : "=f"(m0), "=f"(m1), "=f"(d0), "=f"(d1)
-      : "f"(x0), "f"(x1), "f"(rcp), "f"(RNE_MAGIC));
-}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -155,21 +101,16 @@ __global__ void __launch_bounds__(QT, Q_BLOCKS_PER_SM) quantize_rows_f16_kernel(
           f[2 * j + 1] = p.y;
         }
         if (MODE == BQ_ROUND_F32DIV && normal_scale) {
-          // |x / s| <= d (1 + 2**-11) for a normal scale, so no code needs clamping
-          float dev = 0.0f;
+          // |x / s| <= d (1 + 2**-11) for a normal scale: no code needs
+          // clamping, and the division-free form gives the code exactly
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
-            float d0, d1;
-            code_fast2(f[e], f[e + 1], rcp, m[e], m[e + 1], d0, d1);
-            dev = fmaxf(dev, fmaxf(fabsf(d0), fabsf(d1)));
-          }
-          if (dev > 0.5f - 2.44140625e-4f) {   // rare: a product within 2**-12 of a half-integer
-#pragma unroll
-            for (int e = 0; e < 8; ++e) m[e] = quant_one(f[e], s, rcp, fd, MODE);
+            float r0, r1;
+            code2_fast(f[e], f[e + 1], s, rcp, m[e], m[e + 1], r0, r1);
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) m[e] = quant_one(f[e], s, rcp, fd, MODE);
+          for (int e = 0; e < 8; ++e) m[e] = code_exact(f[e], s, fd, MODE);
         }
         // low bytes of the codes -> two words
         uint32_t packed[2];
@@ -222,11 +163,10 @@ __global__ void __launch_bounds__(256) quantize_rows_generic_kernel(const T* __r
   const int d = qmax_of(bits);
   const __half sh = __float2half_rn(__fdiv_rn(amax, (float)d));
   const float s = __half2float(sh);
-  const float rcp = s == 0.0f ? 0.0f : __frcp_rn(s);
   if (threadIdx.x == 0) scale[row] = sh;
   int8_t* qr = q + row * cols;
   for (int64_t c = threadIdx.x; c < cols; c += blockDim.x)
-    qr[c] = (int8_t)(uint8_t)(code_byte(quant_one(load_as_float(xr + c), s, rcp, (float)d, mode)) & 0xffu);
+    qr[c] = (int8_t)(uint8_t)(code_byte(code_exact(load_as_float(xr + c), s, (float)d, mode)) & 0xffu);
 }
 
 template <int VPT>
@@ -243,7 +183,58 @@ cudaError_t launch_rows_f16(const void* x, int64_t rows, int64_t cols, int64_t l
   return cudaGetLastError();
 }
 
+// Scales only (int8 codes, D = 127), for the fused quantised linear whose
+// GEMM quantises the activations itself: one warp per fp16 row of `cols`
+// elements (a multiple of 8, 16-byte aligned rows), the same absmax and fp16
+// scale as the quantiser kernel.  x is read with ordinary caching so that the
+// GEMM that follows finds it in L2.
+constexpr int RS_WARPS = 8;
+
+__global__ void __launch_bounds__(RS_WARPS * 32) row_scale_f16_kernel(const __half* __restrict__ x, int64_t rows,
+                                                                     int64_t cols, __half* __restrict__ scale) {
+  const int64_t row = (int64_t)blockIdx.x * RS_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * cols);
+  const int nvec = (int)(cols >> 3);
+  __half2 m2[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) m2[u] = __float2half2_rn(0.0f);
+  int i = lane;
+  for (; i + 96 < nvec; i += 128) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = xr[i + 32 * u];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const __half2* h = reinterpret_cast<const __half2*>(&v[u]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m2[u] = __hmax2(m2[u], __habs2(h[j]));
+    }
+  }
+  for (; i < nvec; i += 32) {
+    const uint4 v = xr[i];
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m2[0] = __hmax2(m2[0], __habs2(h[j]));
+  }
+  const __half2 m = __hmax2(__hmax2(m2[0], m2[1]), __hmax2(m2[2], m2[3]));
+  float amax = fmaxf(__low2float(m), __high2float(m));
+  amax = warp_max(amax);
+  if (lane == 0) scale[row] = __float2half_rn(__fdiv_rn(amax, 127.0f));
+}
+
 }  // namespace
+
+cudaError_t launch_row_scale_f16(const void* x, int64_t rows, int64_t cols, uint16_t* scale, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  if (cols == 0) return cudaMemsetAsync(scale, 0, (size_t)rows * sizeof(uint16_t), stream);
+  const int64_t blocks = (rows + RS_WARPS - 1) / RS_WARPS;
+  if (blocks > 0x7fffffffLL || cols % 8 != 0) return cudaErrorInvalidValue;
+  row_scale_f16_kernel<<<(unsigned)blocks, RS_WARPS * 32, 0, stream>>>(static_cast<const __half*>(x), rows, cols,
+                                                                       reinterpret_cast<__half*>(scale));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize(const void* x, int xtype, int64_t rows, int64_t cols, int64_t ld_x, int bits, int mode,
                             int8_t* q, uint16_t* scale, cudaStream_t stream) {

@@ -25,6 +25,7 @@ EXPECTED = sorted([
     "bq_gemm_i8xi4", "bq_gemm_i8xi2", "bq_gemm_f16xi4", "bq_device_status", "bq_set_wait_timeout_ns",
     "bq_gemm_i8xi8_act", "bq_gemm_i8xi4_act", "bq_gemm_i8xi2_act", "bq_gemm_f16xi4_act",
     "bq_gemm_i8xi8_batched", "bq_gemm_i8xi4_batched", "bq_gemm_i8xi2_batched", "bq_gemm_f16xi4_batched",
+    "bq_quantized_linear",
 ])
 
 FAKE = ctypes.c_void_p(0x10000)     # aligned, never dereferenced
@@ -177,6 +178,39 @@ def test_batched_validation(lib):
     g = lib.bq_gemm_f16xi4_batched
     assert g(FAKE, 0, FAKE, 2048, 1, 2, 4, 64, 64, None, 0, 0, FAKE, 256, None) == bq.BQ_ERR_INVALID_ARG  # scale required
     assert g(FAKE, 0, FAKE, 2048, 1, 2, 0, 64, 64, FAKE, 64, 0, FAKE, 0, None) == bq.BQ_OK
+
+
+def test_quantized_linear_validation(lib):
+    f = lib.bq_quantized_linear
+    # (X, M, K, W, bits, layout, N, w_scale, activation, x_scale, Y, stream)
+    ok = dict(X=FAKE, M=4, K=128, W=FAKE, bits=4, layout=1, N=64, ws=FAKE, act=0, xs=FAKE, Y=FAKE)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["X"], a["M"], a["K"], a["W"], a["bits"], a["layout"], a["N"], a["ws"], a["act"], a["xs"],
+                 a["Y"], None)
+
+    assert call(M=-1) == bq.BQ_ERR_INVALID_ARG
+    assert call(bits=3) == bq.BQ_ERR_INVALID_ARG
+    assert call(layout=2) == bq.BQ_ERR_INVALID_ARG
+    assert call(act=3) == bq.BQ_ERR_INVALID_ARG
+    assert call(X=None) == bq.BQ_ERR_INVALID_ARG
+    assert call(xs=None) == bq.BQ_ERR_INVALID_ARG
+    assert call(W=None) == bq.BQ_ERR_INVALID_ARG
+    assert call(ws=None) == bq.BQ_ERR_INVALID_ARG
+    assert call(Y=None) == bq.BQ_ERR_INVALID_ARG
+    assert call(K=96) == bq.BQ_ERR_UNSUPPORTED
+    assert call(N=96) == bq.BQ_ERR_UNSUPPORTED
+    assert call(bits=8, K=8256) == bq.BQ_ERR_UNSUPPORTED       # int8 weights: K <= 8192
+    assert call(bits=4, K=16448) == bq.BQ_ERR_UNSUPPORTED      # 4-bit: K <= 16384
+    # int8 weights, K = 8192 on 32 tiles of 128 x 256: neither K split into ranges of <= 16 k-blocks
+    # nor a grid of CTA pairs that fills the GPU keeps every fp32 chain exact
+    assert call(bits=8, K=8192, M=512, N=2048) == bq.BQ_ERR_UNSUPPORTED
+    assert call(X=FAKE_ODD) == bq.BQ_ERR_ALIGNMENT
+    assert call(xs=FAKE_ODD) == bq.BQ_ERR_ALIGNMENT
+    assert call(Y=FAKE_ODD) == bq.BQ_ERR_ALIGNMENT
+    assert call(M=0, X=None, xs=None) == bq.BQ_OK              # empty
+    assert call(N=0, W=None, ws=None, Y=None, xs=None) == bq.BQ_ERR_INVALID_ARG   # x_scale is still written
 
 
 def test_device_status_null(lib):

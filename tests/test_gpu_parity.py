@@ -73,6 +73,11 @@ def test_quantize_parity(rows, cols, bits, mode):
         x[1] = 0                                               # zero row
         x[2, : min(cols, 3)] = np.float16(178 * 2.0 ** -24)    # subnormal scale, saturation
         x[2, min(cols, 3):] = 0
+    if rows > 3:
+        # exact ties x / s = j + 1/2 with s = 2**-6 (ties to even)
+        d = {8: 127, 4: 7, 2: 1}[bits]
+        x[3] = ((rng.integers(-d, d, size=cols) + 0.5) * 2.0 ** -6).astype(np.float16)
+        x[3, 0] = np.float16(d * 2.0 ** -6)
     q_ref, s_ref = O.quantize_sym(x, bits, "f32div" if mode == bq.ROUND_F32DIV else "bminf_half")
     q, s = bq.bq_quantize_sym(dev(x), bits, mode)
     assert (host(s).view(np.uint16) == s_ref.view(np.uint16)).all()
