@@ -43,6 +43,8 @@ the design notes with its reason):
       overflows for |C| >= 65520; ``dequant_literal_fp16`` reports that).
 * Q11 fp16 x int4 applies the per-channel scale after an exact (float64)
       accumulation.
+* Q16 4-bit weights with a zero point hold unsigned codes u in [0, 15] (the
+      same bit fields as the signed codes) and dequantise as s * (u - z).
 * Q15 a fused activation acts on the dequantised value (after every scale
       product, as the Pallas page applies it to the f32 result of the last
       step before the one downcast) and the result is rounded once to fp16;
@@ -329,6 +331,37 @@ def gemm_f16xq(x: np.ndarray, w_codes: np.ndarray, scale: np.ndarray, act: str =
 def gemm_f16xq_acc(x: np.ndarray, w_codes: np.ndarray) -> np.ndarray:
     """The exact unscaled float64 accumulator of ``gemm_f16xq``."""
     return np.asarray(x, dtype=np.float64) @ np.asarray(w_codes, dtype=np.float64).T
+
+
+# ---------------------------------------------------------------------------
+# 4-bit weights with a per-column zero point  [BitBLAS 实际应用案例 案例2]
+# ---------------------------------------------------------------------------
+def unpack_unsigned(p: np.ndarray, k: int, bits: int, layout: str) -> np.ndarray:
+    """Unsigned codes 0 .. 2**bits - 1 of a packed matrix: the same fields as
+    ``unpack`` reads, taken without sign extension (reading Q16)."""
+    q = unpack(p, k, bits, layout)
+    return (q.astype(np.int16) & ((1 << bits) - 1)).astype(np.uint8)
+
+
+def gemm_f16xu4_zp(x: np.ndarray, u_codes: np.ndarray, scale: np.ndarray, zero_point: np.ndarray,
+                   act: str = "none") -> np.ndarray:
+    """Y[i, j] = fp16( act( sum_k X[i, k] * w[j, k] ) ),  w[j, k] = s[j] * (u[j, k] - z[j]).
+
+    The page's NF4 example takes fp16 activations (M, K), packed weights
+    (N, K // 2) uint8, and a per-column fp16 ``scale`` and ``zero_point``,
+    with fp32 accumulation of the products of the dequantised weights.  Reading
+    Q16: the weight codes are unsigned 4-bit values u in [0, 15] and the
+    dequantisation is the affine w = s * (u - z) with the fp16 zero point z
+    (not necessarily an integer).  Every w is exact in float64, and the sum is
+    a float64 matmul (library step), one rounding to fp16 at the end.
+    """
+    w = scale.astype(np.float64)[:, None] * (np.asarray(u_codes, dtype=np.float64)
+                                             - zero_point.astype(np.float64)[:, None])
+    v = np.asarray(x, dtype=np.float64) @ w.T
+    if act != "none":
+        v = activation(v, act)
+    with np.errstate(over="ignore"):
+        return v.astype(np.float16)
 
 
 # ---------------------------------------------------------------------------

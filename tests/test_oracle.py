@@ -388,6 +388,58 @@ def test_quantized_linear_lossless_activations():
 
 
 # --------------------------------------------------------------------------
+# 4-bit weights with a per-column zero point
+# --------------------------------------------------------------------------
+def _rows(txt, conv=float):
+    return [[conv(v) for v in row.split()] for row in txt.split(";")]
+
+
+def test_zero_point_hand_example():
+    g = load("zero_point_hand_example.txt")
+    x = np.array(_rows(g["x"]), np.float16)
+    u = np.array(_rows(g["u"], int), np.uint8)
+    s = np.array([float(v) for v in g["scale"].split()], np.float16)
+    z = np.array([float(v) for v in g["zero_point"].split()], np.float16)
+    assert O.gemm_f16xu4_zp(x, u, s, z).astype(np.float64).tolist() == _rows(g["y"])
+    assert O.gemm_f16xu4_zp(x, u, s, z, "relu").astype(np.float64).tolist() == _rows(g["y_relu"])
+
+
+def test_zero_point_brute_force_fsum():
+    rng = np.random.default_rng(16)
+    x = W.normal_f16(rng, (3, 48), 1.0)
+    u = rng.integers(0, 16, size=(5, 48)).astype(np.uint8)
+    s = W.uniform_f16(rng, (5,), 1e-3, 1e-2)
+    z = np.array([0, 7.5, 8, 15, 3.3], np.float16)             # integer and fractional zero points
+    y = O.gemm_f16xu4_zp(x, u, s, z)
+    for i in range(3):
+        for j in range(5):
+            # every product is exact in double (at most 11 + 11 + 28 significant bits); fsum rounds once
+            exact = math.fsum(float(x[i, t]) * (float(s[j]) * (int(u[j, t]) - float(z[j]))) for t in range(48))
+            assert float(y[i, j]) == f16(exact)
+
+
+def test_zero_point_eight_is_the_symmetric_form():
+    # u = v + 8 with zero point 8 is the signed 4-bit code v: the symmetric fp16 x int4 product
+    rng = np.random.default_rng(17)
+    x = W.normal_f16(rng, (4, 64), 1.0)
+    v = W.int4_uniform(rng, (6, 64))
+    s = W.uniform_f16(rng, (6,), 1e-3, 1e-2)
+    y = O.gemm_f16xu4_zp(x, (v + 8).astype(np.uint8), s, np.full(6, 8, np.float16))
+    assert (y.view(np.uint16) == O.gemm_f16xq(x, v, s).view(np.uint16)).all()
+
+
+@pytest.mark.parametrize("layout", ["plain", "interleaved"])
+def test_unsigned_codes_round_trip(layout):
+    rng = np.random.default_rng(18)
+    u = rng.integers(0, 16, size=(5, 64)).astype(np.uint8)
+    p = O.pack(u.astype(np.int16).astype(np.int8), 4, layout)   # the low four bits of each code
+    assert (O.unpack_unsigned(p, 64, 4, layout) == u).all()
+    # the fields are the codes' bits: code 15 in the lowest field of a plain byte is 0x0f
+    if layout == "plain":
+        assert O.pack(np.array([[15, 0]], np.int8), 4, "plain")[0, 0] == 0x0F
+
+
+# --------------------------------------------------------------------------
 # Roofline accounting helper
 # --------------------------------------------------------------------------
 def test_roofline_helper_printed_numbers():
