@@ -294,6 +294,37 @@ bq_status bq_quantized_linear(const uint16_t* X, int64_t M, int64_t K, const voi
                               uint16_t* Y, void* stream);
 
 /*
+ * bq_gemm_f16xu4_zp -- fp16 activations times 4-bit weights with a per-column
+ * scale and zero point.  [BitBLAS 实际应用案例 案例2: fp16 A (M, K), packed
+ * weights (N, K // 2) uint8, scale (N,) and zero_point (N,) fp16, fp32
+ * accumulation of the products with the dequantised weights]
+ *
+ *   w[j, k]  = col_scale[j] * (u[j, k] - zero_point[j])   u in [0, 15] unsigned
+ *   Y[i, j]  = fp16_rne( act( sum_k X[i, k] * w[j, k] ) )
+ *   The codes u are packed like the signed 4-bit codes (bq_pack_weights of
+ *   the values 0..15, either layout); zero_point need not be an integer.
+ *   Evaluated as col_scale[j] * (S[i, j] + (8 - zero_point[j]) * row_sum[i])
+ *   with S the fp32 tensor-core sum over X * (u - 8) (in two halves of K, or
+ *   split over a cluster) and the activation applied to that fp32 value.
+ *
+ *   X          device fp16, M x K
+ *   Wp         device packed unsigned 4-bit codes, N x K / 2 bytes
+ *   col_scale, zero_point  device fp16, N
+ *   row_sum    device fp32, M: OUTPUT, row_sum[i] = sum_k X[i, k] in fp32
+ *              (a fixed order), used by the epilogue
+ *   Y          device fp16, M x N: OUTPUT
+ *   Limits: K % 64 == 0, N % 64 == 0, K <= 65536.  Runs on the tensor-core
+ *   kernels for every M (CTA pairs, or K split over a cluster for grids
+ *   smaller than the GPU).  M == 0 is an empty call; N == 0 still writes
+ *   row_sum.
+ *   Errors: INVALID_ARG (null pointers, bad layout or activation),
+ *   ALIGNMENT, UNSUPPORTED, CUDA.
+ */
+bq_status bq_gemm_f16xu4_zp(const uint16_t* X, const uint8_t* Wp, int layout, int64_t M, int64_t N, int64_t K,
+                            const uint16_t* col_scale, const uint16_t* zero_point, int activation, float* row_sum,
+                            uint16_t* Y, void* stream);
+
+/*
  * Device-side wait status.  Every wait inside the tensor-core kernels and the
  * skinny kernel (on a shared-memory mbarrier) is bounded in time.  A wait that gives up records
  * BQ_ERR_TIMEOUT in a device status word, abandons the tile, waits (again

@@ -56,6 +56,8 @@ _SIGNATURES = {
                                               _vp, _c_i64, ctypes.c_int, _vp, _c_i64, _vp]),
     "bq_quantized_linear": (ctypes.c_int, [_vp, _c_i64, _c_i64, _vp, ctypes.c_int, ctypes.c_int, _c_i64, _vp,
                                            ctypes.c_int, _vp, _vp, _vp]),
+    "bq_gemm_f16xu4_zp": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _c_i64, _c_i64, _c_i64, _vp, _vp, ctypes.c_int,
+                                         _vp, _vp, _vp]),
     "bq_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "bq_set_wait_timeout_ns": (_c_i64, [_c_i64]),
 }
@@ -405,6 +407,32 @@ def bq_quantized_linear(X, W, bits, w_scale, layout=LAYOUT_INTERLEAVED, activati
                                    _activation(activation), _ptr(x_scale), _ptr(out), _stream(stream))
     _check(st, "bq_quantized_linear")
     return out, x_scale
+
+
+def bq_gemm_f16xu4_zp(X, Wp, col_scale, zero_point, layout=LAYOUT_INTERLEAVED, activation="none", out=None,
+                      row_sum=None, stream=None):
+    """fp16 X (M, K) times unsigned 4-bit weights Wp (N, K // 2 bytes) with a
+    per-column fp16 scale and zero point.  Returns (Y fp16 (M, N), row_sum
+    fp32 (M,))."""
+    torch = _torch()
+    _need(X, torch.float16, "X", 2)
+    _need(Wp, torch.uint8, "Wp", 2)
+    _need(col_scale, torch.float16, "col_scale", 1)
+    _need(zero_point, torch.float16, "zero_point", 1)
+    M, K = X.shape
+    N = Wp.shape[0]
+    if Wp.shape[1] * 2 != K:
+        raise ValueError("packed width does not match K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    if row_sum is None:
+        row_sum = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _need(out, torch.float16, "out", 2)
+    _need(row_sum, torch.float32, "row_sum", 1)
+    st = lib().bq_gemm_f16xu4_zp(_ptr(X), _ptr(Wp), _layout(layout), M, N, K, _ptr(col_scale), _ptr(zero_point),
+                                 _activation(activation), _ptr(row_sum), _ptr(out), _stream(stream))
+    _check(st, "bq_gemm_f16xu4_zp")
+    return out, row_sum
 
 
 def bq_device_status(reset=True) -> int:

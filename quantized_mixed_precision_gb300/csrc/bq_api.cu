@@ -65,6 +65,9 @@ bq_status run_gemm(GemmArgs g, void* stream) {
   if (g.act == ACT_Q8) {
     // fp16 activations quantised inside the GEMM: the tensor-core kernels only
     e = launch_gemm_tc(g, s);
+  } else if (g.zero_point) {
+    // 4-bit weights with a zero point: the tensor-core kernels for every M
+    e = launch_gemm_tc(g, s);
   } else if (g.act == ACT_I8 && g.bbits == 8) {
     // skinny M, and shapes with no exact tensor-core configuration, use dp4a
     const bool tc_ok = g.M > SKINNY_M && gemm_tc_i8_exact(g);
@@ -318,6 +321,28 @@ bq_status bq_quantized_linear(const uint16_t* X, int64_t M, int64_t K, const voi
   const cudaError_t e = launch_row_scale_f16(X, M, K, x_scale, s);
   if (e != cudaSuccess) return BQ_ERR_CUDA;
   if (N == 0) return BQ_OK;
+  return run_gemm(g, stream);
+}
+
+bq_status bq_gemm_f16xu4_zp(const uint16_t* X, const uint8_t* Wp, int layout, int64_t M, int64_t N, int64_t K,
+                            const uint16_t* col_scale, const uint16_t* zero_point, int activation, float* row_sum,
+                            uint16_t* Y, void* stream) {
+  if (!valid_layout(layout)) return BQ_ERR_INVALID_ARG;
+  if (activation != BQ_ACT_NONE && activation != BQ_ACT_RELU && activation != BQ_ACT_GELU)
+    return BQ_ERR_INVALID_ARG;
+  if (M > 0 && N > 0 && (!col_scale || !zero_point)) return BQ_ERR_INVALID_ARG;
+  if (M > 0 && !row_sum) return BQ_ERR_INVALID_ARG;
+  bq_status st = check_gemm(X, Wp, M, N, K, nullptr, col_scale, Y, MAX_K);
+  if (st != BQ_OK) return st;
+  if (M == 0) return BQ_OK;
+  if (!aligned16(row_sum) || (zero_point && !aligned16(zero_point))) return BQ_ERR_ALIGNMENT;
+  if (K > 0 && !X) return BQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_row_sum_f16(X, M, K, row_sum, s) != cudaSuccess) return BQ_ERR_CUDA;
+  if (N == 0) return BQ_OK;
+  GemmArgs g{X, Wp, ACT_F16, 4, layout, M, N, K, nullptr, col_scale, EPI_F16_COL, Y, activation};
+  g.zero_point = zero_point;
+  g.row_sum = row_sum;
   return run_gemm(g, stream);
 }
 

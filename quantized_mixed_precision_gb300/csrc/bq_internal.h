@@ -10,6 +10,8 @@
 
 namespace bq {
 
+// Streaming multiprocessors of the current device.
+int sm_count();
 // Time limit of bounded device-side waits (nanoseconds).
 int64_t wait_timeout_ns();
 // Address (on the current device) of the status word the bounded waits write.
@@ -23,6 +25,10 @@ cudaError_t launch_quantize(const void* x, int xtype, int64_t rows, int64_t cols
 // Per-row int8 scales (D = 127) of an fp16 matrix with contiguous rows of
 // `cols` elements (cols % 8 == 0): the scales bq_quantize_sym would store.
 cudaError_t launch_row_scale_f16(const void* x, int64_t rows, int64_t cols, uint16_t* scale, cudaStream_t stream);
+
+// fp32 row sums of an fp16 matrix with contiguous rows of `cols` elements
+// (cols % 8 == 0), each summed in a fixed order.
+cudaError_t launch_row_sum_f16(const void* x, int64_t rows, int64_t cols, float* sum, cudaStream_t stream);
 
 cudaError_t launch_pack(const int8_t* q, int64_t n, int64_t k, int bits, int layout, uint8_t* packed,
                         cudaStream_t stream);
@@ -50,6 +56,12 @@ struct GemmArgs {
   int epi;                // EpiKind
   void* c;                // int32 or fp16 (M, N)
   int actfn = BQ_ACT_NONE;  // bq_activation applied before the fp16 rounding
+  // 4-bit weights with a zero point (fp16 activations only): the weights are
+  // unsigned codes u, zero_point is fp16 (N) and row_sum holds the fp32 row
+  // sums of the activations; the epilogue adds (8 - z[j]) * row_sum[i] to the
+  // accumulated sum over x * (u - 8) before the column scale.
+  const uint16_t* zero_point = nullptr;
+  const float* row_sum = nullptr;
 };
 
 // The epilogue argument the GEMM kernels take: the EpiKind in bits 0-3 and

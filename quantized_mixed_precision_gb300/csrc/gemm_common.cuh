@@ -47,9 +47,13 @@ __device__ __forceinline__ void st_chunk(uint8_t* tile, int r, int lc, uint4 v) 
 }
 
 // Convert one 16-byte raw weight piece (row r, piece sub) and store it.
-template <int BBITS, bool INTER>
+// UNS (4-bit only): the nibbles are unsigned codes u in [0, 15]; flipping
+// their top bits makes them the two's-complement codes of u - 8.
+template <int BBITS, bool INTER, bool UNS = false>
 __device__ __forceinline__ void convert_b_piece(uint8_t* tb, int r, int sub, const uint4& v) {
-  const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+  static_assert(!UNS || BBITS == 4, "unsigned codes are 4-bit");
+  constexpr uint32_t FLIP = UNS ? 0x88888888u : 0u;
+  const uint32_t wv[4] = {v.x ^ FLIP, v.y ^ FLIP, v.z ^ FLIP, v.w ^ FLIP};
   if constexpr (BBITS == 8) {
     uint4 o0, o1;
     cvt_i8x4_f16(wv[0], o0.x, o0.y);
@@ -73,6 +77,19 @@ __device__ __forceinline__ void convert_b_piece(uint8_t* tb, int r, int sub, con
       st_chunk(tb, r, 8 * sub + 2 * j, make_uint4(h[0], h[1], h[2], h[3]));
       st_chunk(tb, r, 8 * sub + 2 * j + 1, make_uint4(h[4], h[5], h[6], h[7]));
     }
+  }
+}
+
+// Zero-point epilogue term for 32 consecutive output columns of one row:
+// v[i] + (8 - z[ncol + i]) * rsum, one fp32 fma each.  v is the accumulated
+// sum over x * (u - 8) (the unsigned 4-bit codes u converted as u - 8), so the
+// result is the sum over x * (u - z) before the column scale.
+__device__ __forceinline__ void add_zero_point(float* v, const __half* zero_point, int ncol, float rsum) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __half2 z2 = *reinterpret_cast<const __half2*>(zero_point + ncol + 2 * i);
+    v[2 * i] = __fmaf_rn(__fsub_rn(8.0f, __low2float(z2)), rsum, v[2 * i]);
+    v[2 * i + 1] = __fmaf_rn(__fsub_rn(8.0f, __high2float(z2)), rsum, v[2 * i + 1]);
   }
 }
 

@@ -242,14 +242,18 @@ __device__ __forceinline__ bool pair_drain(int b, uint32_t tmem, uint64_t* chunk
 // separate instantiation, so the kernel without one carries no trace of it).
 // DR: chunked accumulation (int8 x int8, K > 1024); `out` is the output
 // (also the home of the running high parts), used only in that mode.
-template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool AQ, bool ACTV, bool DR>
+// ZP (fp16 activations): unsigned 4-bit weight codes with a per-column zero
+// point; the epilogue adds (8 - zero_point[j]) * row_sum[i].
+template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool AQ, bool ACTV, bool DR, bool ZP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST, AF16, AQ>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, int M, int N, int K,
-                     const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
+                     const __half* __restrict__ row_scale, const __half* __restrict__ col_scale,
+                     const __half* __restrict__ zero_point, const float* __restrict__ row_sum, int epi,
                      void* out, uint64_t timeout_ns, int* status) {
   using C = PairCfg<BBITS, BN, ST, RST, AF16, AQ>;
   static_assert(!DR || (BBITS == 8 && !AF16), "chunked accumulation is for int8 x int8");
+  static_assert(!ZP || (AF16 && BBITS == 4), "zero points are for fp16 x 4-bit");
   // DR: each consumer warp drains at most two 32-column chunks of its quadrant
   static_assert(!DR || BN / 32 <= 2 * (C::CONSUMER_WARPS / 4), "drain chunks per warp");
   const int actfn = epi >> 4;
@@ -516,7 +520,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 #pragma unroll
       for (int i = 0; i < C::NPB; ++i) {
         const int pi = c + i * P_B_THREADS;
-        if (pi < C::B_PIECES) convert_b_piece<BBITS, INTER>(tb, pi % C::HB, pi / C::HB, v[i]);
+        if (pi < C::B_PIECES) convert_b_piece<BBITS, INTER, ZP>(tb, pi % C::HB, pi / C::HB, v[i]);
       }
       fence_proxy_async_smem();   // generic stores -> visible to the tensor core (async proxy)
       // fp16 activations: this CTA's half of the stage is complete once its tile has landed
@@ -567,6 +571,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
           tmem_ld_wait_tied(r2);
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+        }
+        if constexpr (ZP) {
+          if (row < M) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            add_zero_point(v, zero_point, ncol, row_sum[row]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+          }
         }
         // exact integer sums: rint(D), plus 8192 times the drained high parts (DR)
         int ci[32];
@@ -663,7 +677,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool AQ, bool ACTV, bool DR>
+template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool AQ, bool ACTV, bool DR, bool ZP = false>
 cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   using C = PairCfg<BBITS, BN, ST, RST, AF16, AQ>;
   int* status = nullptr;
@@ -683,13 +697,14 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   else
     e = make_map(&mc, g.c, 2, (uint64_t)g.N, (uint64_t)g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, AF16, AQ, ACTV, DR>;
+  auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, AF16, AQ, ACTV, DR, ZP>;
   e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(2 * ((g.M + 2 * PM - 1) / (2 * PM))), (unsigned)((g.N + BN - 1) / BN));
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(ma, mb, mc, (int)g.M, (int)g.N, (int)g.K,
                                               reinterpret_cast<const __half*>(g.row_scale),
-                                              reinterpret_cast<const __half*>(g.col_scale), epi_arg(g), g.c,
+                                              reinterpret_cast<const __half*>(g.col_scale),
+                                              reinterpret_cast<const __half*>(g.zero_point), g.row_sum, epi_arg(g), g.c,
                                               (uint64_t)wait_timeout_ns(), status);
   return cudaGetLastError();
 }
@@ -700,6 +715,13 @@ cudaError_t launch_pair_act(const GemmArgs& g, cudaStream_t stream) {
     // int8 x int8 beyond 16 k-blocks: chunked accumulation keeps the sums exact
     if (g.K > 16 * PK) return launch_pair_t<8, BN, true, ST, RST, false, AQ, ACTV, true>(g, stream);
     return launch_pair_t<8, BN, true, ST, RST, false, AQ, ACTV, false>(g, stream);
+  } else if constexpr (AF16) {
+    if (g.zero_point) {
+      if (g.layout == BQ_LAYOUT_PLAIN) return launch_pair_t<BBITS, BN, false, ST, RST, AF16, AQ, ACTV, false, true>(g, stream);
+      return launch_pair_t<BBITS, BN, true, ST, RST, AF16, AQ, ACTV, false, true>(g, stream);
+    }
+    if (g.layout == BQ_LAYOUT_PLAIN) return launch_pair_t<BBITS, BN, false, ST, RST, AF16, AQ, ACTV, false>(g, stream);
+    return launch_pair_t<BBITS, BN, true, ST, RST, AF16, AQ, ACTV, false>(g, stream);
   } else {
     if (BBITS != 8 && g.layout == BQ_LAYOUT_PLAIN)
       return launch_pair_t<BBITS, BN, false, ST, RST, AF16, AQ, ACTV, false>(g, stream);

@@ -152,7 +152,9 @@ constexpr uint64_t DRAIN_TIMEOUT_NS = 4000000000ull;
 // values loaded straight into the MMA's shared-memory layout.  A_Q_TMEM: fp16
 // values quantised per row to int8 codes (row scales given) by the same
 // converters, which then store the codes into TMEM stages as with A_I8_TMEM.
-enum AMode : int { A_I8_TMEM = 0, A_F16_SMEM = 1, A_Q_TMEM = 2 };
+// A_F16_ZP: as A_F16_SMEM, with unsigned 4-bit weight codes and a per-column
+// zero point (the epilogue adds (8 - z) times the activation row sum).
+enum AMode : int { A_I8_TMEM = 0, A_F16_SMEM = 1, A_Q_TMEM = 2, A_F16_ZP = 3 };
 
 // Converter groups per CTA.
 constexpr int TC_NG = 1;
@@ -161,7 +163,8 @@ constexpr int TC_NG = 1;
 // kb = g (mod NG)), so conversion of consecutive k-blocks overlaps.
 template <int AMODE, int BBITS, int BN, int NACC, int ST, int RST, int NG, int MINB = 1>
 struct Cfg {
-  static constexpr bool A_TMEM = AMODE != A_F16_SMEM;          // A converted into TMEM stages
+  static constexpr bool A_SMEM = AMODE == A_F16_SMEM || AMODE == A_F16_ZP;   // fp16 A straight to the MMA
+  static constexpr bool A_TMEM = !A_SMEM;                      // A converted into TMEM stages
   static constexpr int A_WARPS = A_TMEM ? 4 * NG : 0;
   static constexpr int B_WARPS = 8 * NG;
   static constexpr int MMA_WARP = A_WARPS + B_WARPS;
@@ -183,7 +186,7 @@ struct Cfg {
   static constexpr int A_RAW = AMODE == A_I8_TMEM   ? A_BOX * (RKB / 2)          // raw A per raw stage
                                : AMODE == A_Q_TMEM ? A_KB * RKB
                                                    : 0;
-  static constexpr int A_TILE = AMODE == A_F16_SMEM ? BM * 128 : 0; // fp16 A tile in the MMA stage
+  static constexpr int A_TILE = A_SMEM ? BM * 128 : 0;        // fp16 A tile in the MMA stage
   static constexpr int B_TILE = BN * 128;
   static constexpr int STAGE = A_TILE + B_TILE;
   static constexpr int RSTAGE = (A_RAW + B_RAW + 1023) / 1024 * 1024;
@@ -204,7 +207,8 @@ struct Cfg {
 template <int AMODE, int BBITS, int BN, int NACC, bool INTER, int ST, int RST, int NG, int MINB>
 __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>::THREADS, MINB)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b, int M,
-                   int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale, int epi,
+                   int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale,
+                   const __half* __restrict__ zero_point, const float* __restrict__ row_sum, int epi,
                    void* __restrict__ out, uint64_t timeout_ns, int* status) {
   using C = Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>;
   const int actfn = epi >> 4;
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
       // fp16 A: the producer's expect-tx arrival plus the B converters
-      mbar_init(&full_bar[s], AMODE == A_F16_SMEM ? 1 + B_THREADS : CONSUMERS);
+      mbar_init(&full_bar[s], C::A_SMEM ? 1 + B_THREADS : CONSUMERS);
       mbar_init(&empty_bar[s], 1);
     }
     for (int s = 0; s < RST; ++s) {
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
           tma_load_2d(raw + C::A_RAW, &tmap_b, (kb_lo + kb) * C::B_RAW_ROW, n0, &rfull_bar[rs]);
           issued_groups = grp + 1;
         }
-        if constexpr (AMODE == A_F16_SMEM) {
+        if constexpr (C::A_SMEM) {
           const int s = kb % ST;
           if (!mbar_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) break;
           mbar_arrive_expect_tx(&full_bar[s], BM * BK * 2);
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
       // no TMA write may land after the CTA has exited
       for (int grp = issued_groups > RST ? issued_groups - RST : 0; grp < issued_groups; ++grp)
         mbar_wait(&rfull_bar[grp % RST], (grp / RST) & 1, DRAIN_TIMEOUT_NS, status);
-      if constexpr (AMODE == A_F16_SMEM) {
+      if constexpr (C::A_SMEM) {
         for (int kb = issued_kb > ST ? issued_kb - ST : 0; kb < issued_kb; ++kb)
           mbar_wait(&full_bar[kb % ST], (kb / ST) & 1, DRAIN_TIMEOUT_NS, status);
       }
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
       const uint32_t d = tm + (uint32_t)(slice * BN);
       const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::STAGE + C::A_TILE);
       if (elect_one()) {
-        if constexpr (AMODE == A_F16_SMEM) {
+        if constexpr (C::A_SMEM) {
           const uint64_t adesc = smem_desc_sw128(smem_base + s * C::STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K = +2 in the address field
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
 #pragma unroll
       for (int i = 0; i < C::NPB; ++i) {
         const int pi = c + i * B_THREADS;
-        if (pi < C::B_PIECES) convert_b_piece<BBITS, INTER>(tb, pi % BN, pi / BN, v[i]);
+        if (pi < C::B_PIECES) convert_b_piece<BBITS, INTER, AMODE == A_F16_ZP>(tb, pi % BN, pi / BN, v[i]);
       }
       fence_proxy_async_smem();
       mbar_arrive(&full_bar[s]);
@@ -473,6 +477,9 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
         if (C::A_TMEM && NACC > 1) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __int2float_rn(iv[i]);
+        }
+        if constexpr (AMODE == A_F16_ZP) {
+          if (row_ok && ncol < N) add_zero_point(v, zero_point, ncol, row_sum[row]);
         }
         if (row_ok && ncol < N) {
           if (epi == EPI_I32) {
@@ -585,6 +592,9 @@ __global__ void __launch_bounds__(Cfg<AMODE, BBITS, BN, NACC, ST, RST, NG, MINB>
             for (int i = 0; i < 32; ++i) acc[i] = __int2float_rn(iacc[i]);
           }
           const int ncol = n0 + 32 * c;
+          if constexpr (AMODE == A_F16_ZP) {
+            if (row_ok && ncol < N) add_zero_point(acc, zero_point, ncol, row_sum[row]);
+          }
           if (row_ok && ncol < N) {
             if (epi == EPI_I32) {
               int4* dst = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + (size_t)row * N + ncol);
@@ -673,7 +683,9 @@ cudaError_t launch_t(const GemmArgs& g, int split, cudaStream_t stream) {
   const int epi = epi_arg(g);
   void* out = g.c;
   const uint64_t to = (uint64_t)wait_timeout_ns();
-  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, M, N, K, rsc, csc, epi, out, to, status);
+  const __half* zp = reinterpret_cast<const __half*>(g.zero_point);
+  const float* rsum = g.row_sum;
+  e = cudaLaunchKernelEx(&cfg, kern, ma, mb, M, N, K, rsc, csc, zp, rsum, epi, out, to, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -737,6 +749,10 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, cudaStream_t stream) {
   if (g.act == ACT_F16 && g.bbits == 4) {
     // fp32 chains of at most about half of K: two TMEM slices, or split-K
     const long long tiles = ((g.N + 255) / 256) * ((g.M + BM - 1) / BM);
+    if (g.zero_point) {
+      if (nkb < 2 || choose_split(tiles, nkb) > 1) return launch_layout<A_F16_ZP, 4, 256, 1, 3, 2>(g, stream);
+      return launch_layout<A_F16_ZP, 4, 256, 2, 3, 2>(g, stream);
+    }
     if (nkb < 2 || choose_split(tiles, nkb) > 1) return launch_layout<A_F16_SMEM, 4, 256, 1, 3, 2>(g, stream);
     return launch_layout<A_F16_SMEM, 4, 256, 2, 3, 2>(g, stream);
   }

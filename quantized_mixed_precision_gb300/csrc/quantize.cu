@@ -224,7 +224,40 @@ __global__ void __launch_bounds__(RS_WARPS * 32) row_scale_f16_kernel(const __ha
   if (lane == 0) scale[row] = __float2half_rn(__fdiv_rn(amax, 127.0f));
 }
 
+// Row sums for the zero-point epilogue: one warp per row, each lane sums its
+// 16-byte chunks in fp32 in k order, then a fixed butterfly across the warp.
+__global__ void __launch_bounds__(RS_WARPS * 32) row_sum_f16_kernel(const __half* __restrict__ x, int64_t rows,
+                                                                   int64_t cols, float* __restrict__ sum) {
+  const int64_t row = (int64_t)blockIdx.x * RS_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * cols);
+  const int nvec = (int)(cols >> 3);
+  float acc = 0.0f;
+  for (int i = lane; i < nvec; i += 32) {
+    const uint4 v = xr[i];
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 p = __half22float2(h[j]);
+      acc = __fadd_rn(__fadd_rn(acc, p.x), p.y);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+  if (lane == 0) sum[row] = acc;
+}
+
 }  // namespace
+
+cudaError_t launch_row_sum_f16(const void* x, int64_t rows, int64_t cols, float* sum, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  if (cols == 0) return cudaMemsetAsync(sum, 0, (size_t)rows * sizeof(float), stream);
+  const int64_t blocks = (rows + RS_WARPS - 1) / RS_WARPS;
+  if (blocks > 0x7fffffffLL || cols % 8 != 0) return cudaErrorInvalidValue;
+  row_sum_f16_kernel<<<(unsigned)blocks, RS_WARPS * 32, 0, stream>>>(static_cast<const __half*>(x), rows, cols, sum);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_row_scale_f16(const void* x, int64_t rows, int64_t cols, uint16_t* scale, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;

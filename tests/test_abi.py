@@ -25,7 +25,7 @@ EXPECTED = sorted([
     "bq_gemm_i8xi4", "bq_gemm_i8xi2", "bq_gemm_f16xi4", "bq_device_status", "bq_set_wait_timeout_ns",
     "bq_gemm_i8xi8_act", "bq_gemm_i8xi4_act", "bq_gemm_i8xi2_act", "bq_gemm_f16xi4_act",
     "bq_gemm_i8xi8_batched", "bq_gemm_i8xi4_batched", "bq_gemm_i8xi2_batched", "bq_gemm_f16xi4_batched",
-    "bq_quantized_linear",
+    "bq_quantized_linear", "bq_gemm_f16xu4_zp",
 ])
 
 FAKE = ctypes.c_void_p(0x10000)     # aligned, never dereferenced
@@ -211,6 +211,20 @@ def test_quantized_linear_validation(lib):
     assert call(Y=FAKE_ODD) == bq.BQ_ERR_ALIGNMENT
     assert call(M=0, X=None, xs=None) == bq.BQ_OK              # empty
     assert call(N=0, W=None, ws=None, Y=None, xs=None) == bq.BQ_ERR_INVALID_ARG   # x_scale is still written
+
+
+def test_zero_point_gemm_validation(lib):
+    f = lib.bq_gemm_f16xu4_zp
+    # (X, Wp, layout, M, N, K, col_scale, zero_point, activation, row_sum, Y, stream)
+    assert f(FAKE, FAKE, 2, 4, 64, 128, FAKE, FAKE, 0, FAKE, FAKE, None) == bq.BQ_ERR_INVALID_ARG   # layout
+    assert f(FAKE, FAKE, 1, 4, 64, 128, FAKE, FAKE, 5, FAKE, FAKE, None) == bq.BQ_ERR_INVALID_ARG   # activation
+    assert f(FAKE, FAKE, 1, 4, 64, 128, FAKE, None, 0, FAKE, FAKE, None) == bq.BQ_ERR_INVALID_ARG   # zero point
+    assert f(FAKE, FAKE, 1, 4, 64, 128, None, FAKE, 0, FAKE, FAKE, None) == bq.BQ_ERR_INVALID_ARG   # scale
+    assert f(FAKE, FAKE, 1, 4, 64, 128, FAKE, FAKE, 0, None, FAKE, None) == bq.BQ_ERR_INVALID_ARG   # row sums
+    assert f(FAKE, FAKE, 1, 4, 64, 96, FAKE, FAKE, 0, FAKE, FAKE, None) == bq.BQ_ERR_UNSUPPORTED    # K % 64
+    assert f(FAKE, FAKE, 1, 4, 64, 128, FAKE, FAKE, 0, FAKE_ODD, FAKE, None) == bq.BQ_ERR_ALIGNMENT
+    assert f(FAKE, FAKE, 1, 4, 64, 128, FAKE, FAKE_ODD, 0, FAKE, FAKE, None) == bq.BQ_ERR_ALIGNMENT
+    assert f(None, None, 1, 0, 64, 128, None, None, 0, None, None, None) == bq.BQ_OK                # empty
 
 
 def test_device_status_null(lib):
