@@ -62,6 +62,8 @@ def parse():
     p.add_argument("--impl", choices=["bq", "reference"], default="bq")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-paths", action="store_true")
+    p.add_argument("--profile", choices=sorted(PROFILES),
+                   help="run one workload a few times through the C ABI and exit (for ncu captures)")
     return p.parse_args()
 
 
@@ -444,7 +446,27 @@ def measure_paths(torch, bq, W, roofline, dev, flush, stream, hbm_peak, tc_peak,
     ops = roofline.matmul_ops(1024, 4096, 4096)
     out["i8xi8_rowcol_1024x4096x4096"] = {"ms": ms, "TOPS": ops / (ms * 1e-3) / 1e12,
                                           "tc_frac": ops / (ms * 1e-3) / 1e12 / tc_peak}
-    del Wt, Xt, wq, sw, xq, sx
+    # the fused quantised linear (fp16 X quantised inside the GEMM) beside the two-call path
+    # (bq_quantize_sym of X, then the integer GEMM with both scales), for 8- and 4-bit weights
+    Y = torch.empty((1024, 4096), dtype=torch.float16, device=dev)
+    sxf = torch.empty((1024,), dtype=torch.float16, device=dev)
+    q = torch.empty((1024, 4096), dtype=torch.int8, device=dev)
+    w4q, sw4 = bq.bq_quantize_sym(Wt, 4)
+    w4 = bq.bq_pack_weights(w4q, 4, "interleaved")
+    for bits, wd, swd, gemm in ((8, wq, sw, lambda: bq.bq_gemm_i8xi8(q, wq, row_scale=sxf, col_scale=sw, out=Y)),
+                                (4, w4, sw4, lambda: bq.bq_gemm_i8xi4(q, w4, "interleaved", row_scale=sxf,
+                                                                      col_scale=sw4, out=Y))):
+        ms_f = med(lambda: bq.bq_quantized_linear(Xt, wd, bits, swd, layout="interleaved", out=Y, x_scale=sxf))
+
+        def two_call():
+            bq.bq_quantize_sym(Xt, 8, q=q, scale=sxf)
+            gemm()
+
+        ms_2 = med(two_call)
+        out[f"linear_fused_w{bits}_1024x4096x4096"] = {
+            "ms": ms_f, "TOPS": ops / (ms_f * 1e-3) / 1e12, "two_call_ms": ms_2,
+            "two_call_TOPS": ops / (ms_2 * 1e-3) / 1e12, "launches": 2, "two_call_launches": 2}
+    del Wt, Xt, wq, sw, xq, sx, Y, sxf, q, w4q, sw4, w4
     # INT8 x INT4 256^3 int32
     d0 = W.cfg0()
     A0 = torch.from_numpy(d0["A"]).to(dev)
@@ -484,7 +506,23 @@ def measure_paths(torch, bq, W, roofline, dev, flush, stream, hbm_peak, tc_peak,
         f = roofline.matmul_ops(M, 4096, 11008)
         out[f"f16xi4_M{M}"] = {"ms": ms, "GB/s": b / (ms * 1e-3) / 1e9, "TFLOPS": f / (ms * 1e-3) / 1e12,
                                "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "tc_frac": f / (ms * 1e-3) / 1e12 / tc_peak}
-    del W3, X3
+    # fp16 x unsigned 4-bit with a per-column zero point (codes u = q + 8, zero points in [0, 15] with some
+    # fractional), the same layer and activations
+    rng = np.random.default_rng(0)
+    U3 = bq.bq_pack_weights((torch.from_numpy(d3["W"]).to(dev).to(torch.int16) + 8).to(torch.int8), 4,
+                            "interleaved")
+    z3 = torch.from_numpy((rng.integers(0, 16, size=11008) + rng.uniform(-0.5, 0.5, size=11008))
+                          .astype(np.float16)).to(dev)
+    rs3 = torch.empty((1024,), dtype=torch.float32, device=dev)
+    for M in (1, 64, 1024):
+        Xm = X3[:M].contiguous()
+        ms = med(lambda: bq.bq_gemm_f16xu4_zp(Xm, U3, s3, z3, "interleaved", row_sum=rs3[:M]))
+        b = roofline.matmul_min_bytes(M, 4096, 11008, 16, 4, 16, extra_bytes=4 * 11008 + 4 * M)
+        f = roofline.matmul_ops(M, 4096, 11008)
+        out[f"f16xu4_zp_M{M}"] = {"ms": ms, "GB/s": b / (ms * 1e-3) / 1e9, "TFLOPS": f / (ms * 1e-3) / 1e12,
+                                  "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak,
+                                  "tc_frac": f / (ms * 1e-3) / 1e12 / tc_peak, "launches": 2}
+    del W3, X3, U3, z3, rs3
     # INT8 x ternary, N = K = 8192
     d4 = W.cfg4(M=1024)
     B4 = bq.bq_pack_weights(torch.from_numpy(d4["B"]).to(dev), 2, "interleaved")
@@ -558,8 +596,66 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def _profile_workloads():
+    """Named single workloads, each a callable that sets up its inputs once and
+    returns the step to launch."""
+    def setup(name):
+        import torch
+
+        import quantized_mixed_precision_gb300 as bq
+        from quantized_mixed_precision_gb300 import workloads as W
+        dev = torch.device("cuda")
+        bq.lib()
+        if name in ("gemv_m1", "f16xi4_m64", "zp_m1024"):
+            M = {"gemv_m1": 1, "f16xi4_m64": 64, "zp_m1024": 1024}[name]
+            d = W.cfg3(M=M, source=False)
+            X = torch.from_numpy(d["X"]).to(dev)
+            s = torch.full((11008,), 0.01, dtype=torch.float16, device=dev)
+            if name == "zp_m1024":
+                U = bq.bq_pack_weights((torch.from_numpy(d["W"]).to(dev).to(torch.int16) + 8).to(torch.int8), 4,
+                                       "interleaved")
+                z = torch.full((11008,), 7.5, dtype=torch.float16, device=dev)
+                return lambda: bq.bq_gemm_f16xu4_zp(X, U, s, z, "interleaved")
+            Wp = bq.bq_pack_weights(torch.from_numpy(d["W"]).to(dev), 4, "interleaved")
+            return lambda: bq.bq_gemm_f16xi4(X, Wp, s, "interleaved")
+        if name == "quantize_4096":
+            Wt = torch.from_numpy(W.cfg1(M=1)["W"]).to(dev)
+            q = torch.empty((4096, 4096), dtype=torch.int8, device=dev)
+            sc = torch.empty((4096,), dtype=torch.float16, device=dev)
+            return lambda: bq.bq_quantize_sym(Wt, 8, q=q, scale=sc)
+        if name == "linear_w8_1024":
+            d = W.cfg1()
+            wq, sw = bq.bq_quantize_sym(torch.from_numpy(d["W"]).to(dev), 8)
+            X = torch.from_numpy(d["X"]).to(dev)
+            return lambda: bq.bq_quantized_linear(X, wq, 8, sw)
+        if name == "pair_i8xi4_4096":
+            d = W.cfg2()
+            A = torch.from_numpy(d["A"]).to(dev)
+            Bp = bq.bq_pack_weights(torch.from_numpy(d["B"]).to(dev), 4, "interleaved")
+            sc = torch.from_numpy(d["scale"]).to(dev)
+            return lambda: bq.bq_gemm_i8xi4(A, Bp, "interleaved", col_scale=sc)
+        raise ValueError(name)
+    return setup
+
+
+PROFILES = ("gemv_m1", "f16xi4_m64", "quantize_4096", "linear_w8_1024", "zp_m1024", "pair_i8xi4_4096")
+
+
+def run_profile(name, launches=3):
+    import torch
+    step = _profile_workloads()(name)
+    for _ in range(2 + launches):
+        step()
+    torch.cuda.synchronize()
+    import quantized_mixed_precision_gb300 as bq
+    print(json.dumps({"profile": name, "launches": 2 + launches, "status": bq.bq_device_status(reset=True)}))
+
+
 def main():
     args = parse()
+    if args.profile:
+        run_profile(args.profile)
+        return
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)

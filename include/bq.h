@@ -304,8 +304,8 @@ bq_status bq_quantized_linear(const uint16_t* X, int64_t M, int64_t K, const voi
  *   The codes u are packed like the signed 4-bit codes (bq_pack_weights of
  *   the values 0..15, either layout); zero_point need not be an integer.
  *   Evaluated as col_scale[j] * (S[i, j] + (8 - zero_point[j]) * row_sum[i])
- *   with S the fp32 tensor-core sum over X * (u - 8) (in two halves of K, or
- *   split over a cluster) and the activation applied to that fp32 value.
+ *   with S the fp32 sum over X * (u - 8) of the fp16 x int4 kernels (the
+ *   same chains) and the activation applied to that fp32 value.
  *
  *   X          device fp16, M x K
  *   Wp         device packed unsigned 4-bit codes, N x K / 2 bytes
@@ -313,10 +313,11 @@ bq_status bq_quantized_linear(const uint16_t* X, int64_t M, int64_t K, const voi
  *   row_sum    device fp32, M: OUTPUT, row_sum[i] = sum_k X[i, k] in fp32
  *              (a fixed order), used by the epilogue
  *   Y          device fp16, M x N: OUTPUT
- *   Limits: K % 64 == 0, N % 64 == 0, K <= 65536.  Runs on the tensor-core
- *   kernels for every M (CTA pairs, or K split over a cluster for grids
- *   smaller than the GPU).  M == 0 is an empty call; N == 0 still writes
- *   row_sum.
+ *   Limits: K % 64 == 0, N % 64 == 0, K <= 65536.  Dispatch as bq_gemm_f16xi4
+ *   (M <= 16 the skinny kernel while 16 staged weight rows fit in 64 KB,
+ *   16 < M <= 128 the kernel with the weights as the MMA's A operand, else
+ *   the CTA-pair or split-K tensor-core kernels).  M == 0 is an empty call;
+ *   N == 0 still writes row_sum.
  *   Errors: INVALID_ARG (null pointers, bad layout or activation),
  *   ALIGNMENT, UNSUPPORTED, CUDA.
  */

@@ -66,8 +66,10 @@ bq_status run_gemm(GemmArgs g, void* stream) {
     // fp16 activations quantised inside the GEMM: the tensor-core kernels only
     e = launch_gemm_tc(g, s);
   } else if (g.zero_point) {
-    // 4-bit weights with a zero point: the tensor-core kernels for every M
-    e = launch_gemm_tc(g, s);
+    // 4-bit weights with a zero point: the same M buckets as fp16 x int4
+    if (g.M <= SKINNY_M && gemv_zp_fits(g.M, g.K)) e = launch_gemv_mma(g, s);
+    else if (gemm_swap_applies(g)) e = launch_gemm_swap(g, s);
+    else e = launch_gemm_tc(g, s);
   } else if (g.act == ACT_I8 && g.bbits == 8) {
     // skinny M, and shapes with no exact tensor-core configuration, use dp4a
     const bool tc_ok = g.M > SKINNY_M && gemm_tc_i8_exact(g);

@@ -80,6 +80,8 @@ cudaError_t set_smem_once(Kernel kern, int bytes) {
 // Skinny-M path (M <= 16): one pass over the weights, legacy mma.sync fp16.
 // gemv_fits tells whether its staged activations fit in shared memory.
 bool gemv_fits(int64_t M, int64_t K, int bbits);
+// The same for fp16 x 4-bit weights with zero points (bulk variant only).
+bool gemv_zp_fits(int64_t M, int64_t K);
 cudaError_t launch_gemv_mma(const GemmArgs& g, cudaStream_t stream);
 // int8 x int8 with exact int32 dp4a accumulation (any M).
 cudaError_t launch_gemm_dp4a(const GemmArgs& g, cudaStream_t stream);

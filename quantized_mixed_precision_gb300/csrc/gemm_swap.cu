@@ -79,12 +79,17 @@ struct SwapCfg {
   static_assert(SMEM <= 232448, "shared memory");
 };
 
-template <int BBITS, int MN, bool INTER>
+// ZP (4-bit): unsigned weight codes with a per-column zero point; the
+// epilogue adds (8 - zero_point[n]) * row_sum[m] before the column scale.
+template <int BBITS, int MN, bool INTER, bool ZP = false>
 __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
     gemm_swap_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x, int M,
                      int N, int K, const __half* __restrict__ row_scale, const __half* __restrict__ col_scale,
-                     int epi, void* __restrict__ out, uint64_t timeout_ns, int* status) {
+                     const __half* __restrict__ zero_point, const float* __restrict__ row_sum, int epi,
+                     void* __restrict__ out, uint64_t timeout_ns, int* status) {
   using C = SwapCfg<BBITS, MN>;
+  static_assert(!ZP || BBITS == 4, "zero points are for 4-bit weights");
+  constexpr uint32_t FLIP = ZP ? 0x88888888u : 0u;   // unsigned codes u -> two's-complement u - 8
   const int actfn = epi >> 4;
   epi &= 15;
   extern __shared__ uint8_t smem_raw[];
@@ -217,7 +222,8 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
         const uint4 v1 = *reinterpret_cast<const uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4));
         if ((kb % C::RKB) + SW_NG >= C::RKB || kb + SW_NG >= nkb)
           mbar_arrive_after_loads(&rempty_bar[rs], fold4(v0) ^ fold4(v1), rzero);
-        const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        const uint32_t wv[8] = {v0.x ^ FLIP, v0.y ^ FLIP, v0.z ^ FLIP, v0.w ^ FLIP,
+                                v1.x ^ FLIP, v1.y ^ FLIP, v1.z ^ FLIP, v1.w ^ FLIP};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           uint32_t t4[4];
@@ -260,6 +266,7 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
       const int n = n0 + r;
       if (acc_ok) {
         const float cs = (epi != EPI_I32 && n < N) ? __half2float(col_scale[n]) : 0.0f;
+        const float zc = (ZP && n < N) ? __fsub_rn(8.0f, __half2float(zero_point[n])) : 0.0f;
 #pragma unroll 1
         for (int c = 0; c < MN / 32 + (MN % 32 ? 1 : 0); ++c) {
           uint32_t v[32];
@@ -277,7 +284,8 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
           for (int i = 0; i < 32; ++i) {
             const int m = 32 * c + i;
             if (m >= M) break;
-            const float acc = __uint_as_float(v[i]);
+            float acc = __uint_as_float(v[i]);
+            if constexpr (ZP) acc = __fmaf_rn(zc, row_sum[m], acc);
             const size_t o = (size_t)m * N + n;
             if (epi == EPI_I32) {
               static_cast<int32_t*>(out)[o] = __float2int_rn(acc);
@@ -301,7 +309,7 @@ __global__ void __launch_bounds__(SwapCfg<BBITS, MN>::THREADS, 1)
   }
 }
 
-template <int BBITS, int MN, bool INTER>
+template <int BBITS, int MN, bool INTER, bool ZP = false>
 cudaError_t launch_swap_t(const GemmArgs& g, cudaStream_t stream) {
   using C = SwapCfg<BBITS, MN>;
   int* status = nullptr;
@@ -313,7 +321,7 @@ cudaError_t launch_swap_t(const GemmArgs& g, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = make_map(&mx, g.a, 2, (uint64_t)g.K, (uint64_t)g.M, SW_K, MN, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  auto kern = gemm_swap_kernel<BBITS, MN, INTER>;
+  auto kern = gemm_swap_kernel<BBITS, MN, INTER, ZP>;
   e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -332,13 +340,21 @@ cudaError_t launch_swap_t(const GemmArgs& g, cudaStream_t stream) {
   const int epi = epi_arg(g);
   void* out = g.c;
   const uint64_t to = (uint64_t)wait_timeout_ns();
-  e = cudaLaunchKernelEx(&cfg, kern, mw, mx, M, N, K, rsc, csc, epi, out, to, status);
+  const __half* zp = reinterpret_cast<const __half*>(g.zero_point);
+  const float* rsum = g.row_sum;
+  e = cudaLaunchKernelEx(&cfg, kern, mw, mx, M, N, K, rsc, csc, zp, rsum, epi, out, to, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <int BBITS, int MN>
 cudaError_t launch_swap_layout(const GemmArgs& g, cudaStream_t stream) {
+  if constexpr (BBITS == 4) {
+    if (g.zero_point) {
+      if (g.layout == BQ_LAYOUT_PLAIN) return launch_swap_t<4, MN, false, true>(g, stream);
+      return launch_swap_t<4, MN, true, true>(g, stream);
+    }
+  }
   if (g.layout == BQ_LAYOUT_PLAIN) return launch_swap_t<BBITS, MN, false>(g, stream);
   return launch_swap_t<BBITS, MN, true>(g, stream);
 }

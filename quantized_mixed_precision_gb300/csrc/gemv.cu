@@ -65,9 +65,11 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int BBITS, bool INTER>
+// UNS: unsigned 4-bit codes u, converted as u - 8 (top bits flipped).
+template <int BBITS, bool INTER, bool UNS = false>
 __device__ __forceinline__ void convert_word(uint32_t w, uint32_t (&h)[GemvCfg<BBITS>::PW]) {
   if constexpr (BBITS == 4) {
+    if constexpr (UNS) w ^= 0x88888888u;
     cvt_i4x8_f16(INTER ? w : plain_to_inter_i4(w), h);
   } else {
     cvt_i2x16_f16(INTER ? w : plain_to_inter_i2(w), h);
@@ -288,13 +290,18 @@ __device__ __forceinline__ uint4 load_x8(const uint8_t* xr, int k0, bool live) {
 // in shared memory after the weights: each warp copies its K range of every
 // row once (one bulk copy per row), instead of every warp of every SM
 // re-reading the same few L2 lines at each step.
-template <int BBITS, int ACT, int NB, bool INTER, bool FULL, bool XS>
+// ZP (fp16 x 4-bit): unsigned weight codes with a per-column zero point; the
+// epilogue adds (8 - zero_point[n]) * row_sum[m] before the column scale.
+template <int BBITS, int ACT, int NB, bool INTER, bool FULL, bool XS, bool ZP = false>
 __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* __restrict__ act,
                                                                     const uint8_t* __restrict__ w, int M, int N, int K,
                                                                     const __half* __restrict__ row_scale,
-                                                                    const __half* __restrict__ col_scale, int epi,
+                                                                    const __half* __restrict__ col_scale,
+                                                                    const __half* __restrict__ zero_point,
+                                                                    const float* __restrict__ row_sum, int epi,
                                                                     void* __restrict__ out, uint64_t timeout_ns,
                                                                     int* status) {
+  static_assert(!ZP || (BBITS == 4 && ACT == ACT_F16), "zero points are for fp16 x 4-bit");
   using C = GemvCfg<BBITS>;
   const int actfn = epi >> 4;
   epi &= 15;
@@ -407,8 +414,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint32_t ha[C::PW], hb[C::PW];
-      convert_word<BBITS, INTER>(wa[i], ha);
-      convert_word<BBITS, INTER>(wb[i], hb);
+      convert_word<BBITS, INTER, ZP>(wa[i], ha);
+      convert_word<BBITS, INTER, ZP>(wb[i], hb);
 #pragma unroll
       for (int c = 0; c < C::PW / 4; ++c) {
         const int j = i * (C::PW / 4) + c;
@@ -441,6 +448,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
       if (epi == EPI_I32) {
         static_cast<int32_t*>(out)[o] = __float2int_rn(acc);
       } else {
+        if constexpr (ZP) acc = __fmaf_rn(__fsub_rn(8.0f, __half2float(zero_point[n])), row_sum[m], acc);
         float v = __fmul_rn(acc, __half2float(col_scale[n]));
         if (epi == EPI_F16_ROWCOL) v = __fmul_rn(v, __half2float(row_scale[m]));
         v = apply_act(v, actfn);
@@ -450,13 +458,13 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   }
 }
 
-template <int BBITS, int ACT, int NB, bool INTER, bool FULL, bool XS>
+template <int BBITS, int ACT, int NB, bool INTER, bool FULL, bool XS, bool ZP = false>
 cudaError_t launch_bulk(const GemmArgs& g, cudaStream_t stream) {
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
   const int smem = gemv_bulk_smem<BBITS>((int)g.K) + (XS ? gemv_x_bytes<ACT>(g.M, g.K) : 0);
-  auto kern = gemv_bulk_kernel<BBITS, ACT, NB, INTER, FULL, XS>;
+  auto kern = gemv_bulk_kernel<BBITS, ACT, NB, INTER, FULL, XS, ZP>;
   if (smem > 48 * 1024) {
     e = set_smem_once(kern, smem);
     if (e != cudaSuccess) return e;
@@ -479,7 +487,9 @@ cudaError_t launch_bulk(const GemmArgs& g, cudaStream_t stream) {
   int epi = epi_arg(g);
   void* c = g.c;
   uint64_t to = (uint64_t)wait_timeout_ns();
-  e = cudaLaunchKernelEx(&cfg, kern, a, b, M, N, K, rsc, csc, epi, c, to, status);
+  const __half* zp = reinterpret_cast<const __half*>(g.zero_point);
+  const float* rsum = g.row_sum;
+  e = cudaLaunchKernelEx(&cfg, kern, a, b, M, N, K, rsc, csc, zp, rsum, epi, c, to, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -496,6 +506,22 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
       g.a, static_cast<const uint8_t*>(g.b), (int)g.M, (int)g.N, (int)g.K,
       reinterpret_cast<const __half*>(g.row_scale), reinterpret_cast<const __half*>(g.col_scale), epi_arg(g), g.c);
   return cudaGetLastError();
+}
+
+// fp16 x unsigned 4-bit with zero points: the bulk variant only (gemv_zp_fits)
+cudaError_t launch_bulk_zp(const GemmArgs& g, cudaStream_t stream) {
+  const bool inter = g.layout == BQ_LAYOUT_INTERLEAVED;
+  const bool full = g.K % GemvCfg<4>::STEP == 0;
+  if (g.M <= 8) {
+    if (full) return inter ? launch_bulk<4, ACT_F16, 1, true, true, false, true>(g, stream)
+                           : launch_bulk<4, ACT_F16, 1, false, true, false, true>(g, stream);
+    return inter ? launch_bulk<4, ACT_F16, 1, true, false, false, true>(g, stream)
+                 : launch_bulk<4, ACT_F16, 1, false, false, false, true>(g, stream);
+  }
+  if (full) return inter ? launch_bulk<4, ACT_F16, 2, true, true, false, true>(g, stream)
+                         : launch_bulk<4, ACT_F16, 2, false, true, false, true>(g, stream);
+  return inter ? launch_bulk<4, ACT_F16, 2, true, false, false, true>(g, stream)
+               : launch_bulk<4, ACT_F16, 2, false, false, false, true>(g, stream);
 }
 
 template <int BBITS, int ACT>
@@ -534,7 +560,15 @@ bool gemv_fits(int64_t M, int64_t K, int bbits) {
   return M >= 1 && M <= 16 && bytes <= 200 * 1024;
 }
 
+bool gemv_zp_fits(int64_t M, int64_t K) {
+  return M >= 1 && M <= 16 && gemv_bulk_smem<4>((int)K) <= 64 * 1024;
+}
+
 cudaError_t launch_gemv_mma(const GemmArgs& g, cudaStream_t stream) {
+  if (g.zero_point) {
+    if (g.act != ACT_F16 || g.bbits != 4 || !gemv_zp_fits(g.M, g.K)) return cudaErrorInvalidValue;
+    return launch_bulk_zp(g, stream);
+  }
   if (!gemv_fits(g.M, g.K, g.bbits)) return cudaErrorInvalidValue;
   if (g.bbits == 4) {
     return g.act == ACT_F16 ? launch_bits_act<4, ACT_F16>(g, stream) : launch_bits_act<4, ACT_I8>(g, stream);

@@ -54,7 +54,8 @@ def check_row_sum(rs, x):
     assert (np.abs(host(rs).astype(np.float64) - exact) <= bound).all()
 
 
-# M spans the split-K single-CTA kernel (small grids), and CTA pairs; ragged M and both layouts
+# M spans every bucket: the skinny kernel (M <= 16), the kernel with the weights as the MMA's A operand
+# (16 < M <= 128), the split-K single-CTA kernel and CTA pairs; ragged M and both layouts
 SHAPES = [(1, 4096, 4096, "interleaved"), (5, 1024, 512, "plain"), (17, 2048, 1024, "interleaved"),
           (64, 11008, 4096, "interleaved"), (130, 4096, 2048, "plain"), (600, 8192, 512, "interleaved"),
           (1000, 4096, 1024, "plain")]
@@ -72,7 +73,7 @@ def test_zero_point_parity(M, N, K, layout):
     check_row_sum(rs, x)
 
 
-@pytest.mark.parametrize("M,N,K", [(3, 1024, 512), (200, 4096, 1024), (600, 8192, 512)])
+@pytest.mark.parametrize("M,N,K", [(3, 1024, 512), (40, 4096, 1024), (200, 4096, 1024), (600, 8192, 512)])
 def test_zero_point_eight_equals_symmetric_path(M, N, K):
     rng = np.random.default_rng(M)
     x = W.normal_f16(rng, (M, K), 1.0)
@@ -83,8 +84,8 @@ def test_zero_point_eight_equals_symmetric_path(M, N, K):
     y_zp, _ = bq.bq_gemm_f16xu4_zp(xd, pack_u((v + 8).astype(np.uint8), "interleaved"), sd,
                                    dev(np.full(N, 8, np.float16)))
     torch.cuda.synchronize()
-    if M > 16:   # both on the tensor-core kernels: identical sums, zero correction
-        assert torch.equal(y_zp.view(torch.int16), y_sym.view(torch.int16))
+    # the same kernel family at every M: identical sums, and a zero correction term
+    assert torch.equal(y_zp.view(torch.int16), y_sym.view(torch.int16))
     y_ref = O.gemm_f16xq(x, v, s)
     assert_f16_close(host(y_zp), y_ref, s[None, :].astype(np.float64), "zp8")
 
