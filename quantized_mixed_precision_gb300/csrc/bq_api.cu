@@ -84,10 +84,21 @@ bq_status run_gemm(GemmArgs g, void* stream) {
   return from_cuda(e);
 }
 
+// Whether run_gemm sends this (unbatched) problem, its epilogue kind already
+// set, to the CTA-pair kernel.
+bool routes_to_pair(const GemmArgs& g) {
+  if (g.act == ACT_Q8 || g.zero_point || g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
+  if (g.act == ACT_I8 && g.bbits == 8) return g.M > SKINNY_M && gemm_pair_bn(g) != 0;
+  if (gemm_swap_applies(g)) return false;
+  if (g.M <= SKINNY_M && gemv_fits(g.M, g.K, g.bbits)) return false;
+  return gemm_pair_bn(g) != 0;
+}
+
 // Batched calls: item b uses every pointer advanced by b times its stride
 // (in bytes here; 0 broadcasts).  Validates once for all items -- the items
 // differ from the first only by offsets that are multiples of 16 bytes --
-// then launches them in order.
+// then launches them: as one grid on the CTA-pair kernel where that kernel
+// serves the shape, else one after another.
 bq_status run_batched(const GemmArgs& g, int64_t batch, int64_t sa, int64_t sb, int64_t srs, int64_t scs,
                       int64_t sc, int64_t max_k, void* stream) {
   if (batch < 0 || sa < 0 || sb < 0 || srs < 0 || scs < 0 || sc < 0) return BQ_ERR_INVALID_ARG;
@@ -102,6 +113,23 @@ bq_status run_batched(const GemmArgs& g, int64_t batch, int64_t sa, int64_t sb, 
     if (sa > MAX_STRIDE || sb > MAX_STRIDE || srs > MAX_STRIDE || scs > MAX_STRIDE || sc > MAX_STRIDE ||
         batch > MAX_BATCH)
       return BQ_ERR_UNSUPPORTED;
+  }
+  // Items that run on the CTA-pair kernel share one launch (grid z = item) when
+  // every strided operand's items do not overlap (3-D tensor maps).
+  GemmArgs gb = g;
+  gb.epi = g.col_scale ? (g.row_scale ? EPI_F16_ROWCOL : EPI_F16_COL) : EPI_I32;
+  if (batch > 1 && g.K > 0 && routes_to_pair(gb)) {
+    const int64_t a_bytes = g.M * g.K * (g.act == ACT_F16 ? 2 : 1);
+    const int64_t b_bytes = g.N * g.K * g.bbits / 8;
+    if ((sa == 0 || sa >= a_bytes) && (sb == 0 || sb >= b_bytes)) {
+      gb.batch = batch;
+      gb.sa = sa;
+      gb.sb = sb;
+      gb.srs = g.row_scale ? srs : 0;
+      gb.scs = g.col_scale ? scs : 0;
+      gb.sc = sc;
+      return from_cuda(launch_gemm_pair(gb, gemm_pair_bn(gb), static_cast<cudaStream_t>(stream)));
+    }
   }
   for (int64_t b = 0; b < batch; ++b) {
     GemmArgs gi = g;

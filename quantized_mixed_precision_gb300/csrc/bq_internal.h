@@ -62,6 +62,10 @@ struct GemmArgs {
   // accumulated sum over x * (u - 8) before the column scale.
   const uint16_t* zero_point = nullptr;
   const float* row_sum = nullptr;
+  // Batched launch on the CTA-pair kernel (grid z = item): byte strides
+  // between items (0 broadcasts an operand); batch 1 is an ordinary call.
+  int64_t batch = 1;
+  int64_t sa = 0, sb = 0, srs = 0, scs = 0, sc = 0;
 };
 
 // The epilogue argument the GEMM kernels take: the EpiKind in bits 0-3 and

@@ -16,6 +16,11 @@ namespace bq {
 // written by stores.
 cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_elems, uint64_t rows, uint32_t box_x,
                      uint32_t box_rows, CUtensorMapSwizzle swz);
+// The same over `batch` matrices `item_stride` bytes apart: always a 3-D map
+// (third coordinate = batch item, box depth 1), also for one item, so that a
+// kernel's 3-D copies may use it; load and store only with 3-D copies.
+cudaError_t make_map3(CUtensorMap* map, const void* base, int elem, uint64_t row_elems, uint64_t rows, uint64_t batch,
+                      uint64_t item_stride, uint32_t box_x, uint32_t box_rows, CUtensorMapSwizzle swz);
 // Streaming multiprocessors of the current device.
 int sm_count();
 // Split-K factor the single-CTA kernel uses for `tiles` 128-row tiles of nkb

@@ -147,6 +147,22 @@ struct PairCfg {
   static_assert((3 * ST + 2 * RST + 3) * 8 + 4 <= 256, "barrier area");
 };
 
+// Batched launch (grid z = item): element strides of the scales, the byte
+// stride of the output, and whether A and B have one matrix per item (else
+// every item reads item 0's; their tensor maps then hold one item).
+struct PairBatch {
+  int64_t srs, scs, sc;
+  int za_on, zb_on;
+  int on;   // batched: 3-D tensor maps; otherwise the 2-D maps of one matrix
+};
+
+// A tile load through a 2-D map, or a 3-D map at batch item z.
+__device__ __forceinline__ void tma_load_item(void* dst, const void* tmap, int x, int y, int z, bool b3,
+                                              uint64_t* bar) {
+  if (b3) tma_load_3d(dst, tmap, x, y, z, bar);
+  else tma_load_2d(dst, tmap, x, y, bar);
+}
+
 // True if the 32 consecutive output elements at element offset `off` lie
 // inside the M x N output; otherwise records BQ_DIAG_RANGE (a self-check of
 // the chunked accumulation's bookkeeping) and the caller skips the access.
@@ -250,7 +266,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
                      const __grid_constant__ CUtensorMap tmap_c, int M, int N, int K,
                      const __half* __restrict__ row_scale, const __half* __restrict__ col_scale,
                      const __half* __restrict__ zero_point, const float* __restrict__ row_sum, int epi,
-                     void* out, uint64_t timeout_ns, int* status) {
+                     void* out, const PairBatch bt, uint64_t timeout_ns, int* status) {
   using C = PairCfg<BBITS, BN, ST, RST, AF16, AQ>;
   static_assert(!DR || (BBITS == 8 && !AF16), "chunked accumulation is for int8 x int8");
   static_assert(!ZP || (AF16 && BBITS == 4), "zero points are for fp16 x 4-bit");
@@ -274,6 +290,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
+  // batch item: its scales and output; A and B through the third map coordinate
+  const int z = (int)blockIdx.z;
+  const int za = bt.za_on ? z : 0, zb = bt.zb_on ? z : 0;
+  if (row_scale) row_scale += z * bt.srs;
+  if (col_scale) col_scale += z * bt.scs;
+  out = static_cast<uint8_t*>(out) + z * bt.sc;
   const int m0 = (int)(blockIdx.x >> 1) * (2 * PM) + (int)rank * PM;   // this CTA's tile rows
   const int n0 = blockIdx.y * BN;                                      // the pair's output columns
   const int nb0 = n0 + (int)rank * C::HB;                              // this CTA's weight rows
@@ -343,13 +365,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
           if constexpr (AQ) {
 #pragma unroll
             for (int b = 0; b < C::RKB; ++b)
-              tma_load_2d(raw + b * C::A_KB, &tmap_a, (kb + b) * PK, m0, &rfull_bar[rs]);
+              tma_load_item(raw + b * C::A_KB, &tmap_a, (kb + b) * PK, m0, za, bt.on, &rfull_bar[rs]);
           } else if constexpr (!AF16) {
 #pragma unroll
             for (int b = 0; b < C::RKB / 2; ++b)
-              tma_load_2d(raw + b * C::A_BOX, &tmap_a, (kb + 2 * b) * PK, m0, &rfull_bar[rs]);
+              tma_load_item(raw + b * C::A_BOX, &tmap_a, (kb + 2 * b) * PK, m0, za, bt.on, &rfull_bar[rs]);
           }
-          tma_load_2d(raw + C::A_RAW, &tmap_b, kb * C::B_RAW_ROW, nb0, &rfull_bar[rs]);
+          tma_load_item(raw + C::A_RAW, &tmap_b, kb * C::B_RAW_ROW, nb0, zb, bt.on, &rfull_bar[rs]);
           issued = grp + 1;
         }
         if constexpr (AF16) {
@@ -357,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
           const int s = kb % ST;
           if (!mbar_wait(&empty_bar[s], ((kb / ST) & 1) ^ 1, timeout_ns, status)) break;
           mbar_arrive_expect_tx(&afull_bar[s], C::A_TILE);
-          tma_load_2d(smem + s * C::STAGE, &tmap_a, kb * PK, m0, &afull_bar[s]);
+          tma_load_item(smem + s * C::STAGE, &tmap_a, kb * PK, m0, za, bt.on, &afull_bar[s]);
           issued_a = kb + 1;
         }
       }
@@ -655,7 +677,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         if constexpr (DR) asm volatile("fence.proxy.async.global;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmap_c, stg, ncol, row0);   // rows past M are not written
+          if (bt.on) tma_store_3d(&tmap_c, stg, ncol, row0, z);   // rows past M are not written
+          else tma_store_2d(&tmap_c, stg, ncol, row0);
           bulk_commit_group();
         }
       }
@@ -684,28 +707,42 @@ cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
   CUtensorMap ma, mb, mc;
+  // A batched launch copies with 3-D instructions through 3-D maps for all
+  // three operands (the batch item as the third coordinate; a broadcast
+  // operand's map holds one item); a single call uses 2-D maps and copies.
+  // The rank of every map must match bt.on, the kernel's choice of copy.
+  const uint64_t nb = (uint64_t)(g.batch < 1 ? 1 : g.batch);
+  const bool b3 = nb > 1;
+  const uint64_t na = g.sa ? nb : 1, nbw = g.sb ? nb : 1;
+  auto map = [&](CUtensorMap* m, const void* base, int elem, uint64_t row_elems, uint64_t rows, uint64_t items,
+                 int64_t stride, uint32_t bx, uint32_t by, CUtensorMapSwizzle swz) {
+    return b3 ? make_map3(m, base, elem, row_elems, rows, items, (uint64_t)stride, bx, by, swz)
+              : make_map(m, base, elem, row_elems, rows, bx, by, swz);
+  };
   if (AF16 || AQ)   // one k-block of fp16 rows: 128 bytes, the MMA's (or the converters') 128B swizzle
-    e = make_map(&ma, g.a, 2, (uint64_t)g.K, (uint64_t)g.M, PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
+    e = map(&ma, g.a, 2, (uint64_t)g.K, (uint64_t)g.M, na, g.sa, PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
   else        // two k-blocks of int8 rows
-    e = make_map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, 2 * PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
+    e = map(&ma, g.a, 1, (uint64_t)g.K, (uint64_t)g.M, na, g.sa, 2 * PK, PM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  e = make_map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, C::B_BOX_X, C::HB, raw_swizzle(C::B_BOX_X));
+  e = map(&mb, g.b, 1, (uint64_t)g.K * BBITS / 8, (uint64_t)g.N, nbw, g.sb, C::B_BOX_X, C::HB,
+          raw_swizzle(C::B_BOX_X));
   if (e != cudaSuccess) return e;
   // output boxes of 32 x 32: int32 rows of 128 bytes, fp16 rows of 64 bytes
   if (g.epi == EPI_I32)
-    e = make_map(&mc, g.c, 4, (uint64_t)g.N, (uint64_t)g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    e = map(&mc, g.c, 4, (uint64_t)g.N, (uint64_t)g.M, nb, g.sc, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   else
-    e = make_map(&mc, g.c, 2, (uint64_t)g.N, (uint64_t)g.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    e = map(&mc, g.c, 2, (uint64_t)g.N, (uint64_t)g.M, nb, g.sc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
+  const PairBatch bt{g.srs / 2, g.scs / 2, g.sc, g.sa != 0, g.sb != 0, b3 ? 1 : 0};
   auto kern = gemm_pair_kernel<BBITS, BN, INTER, ST, RST, AF16, AQ, ACTV, DR, ZP>;
   e = set_smem_once(kern, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)(2 * ((g.M + 2 * PM - 1) / (2 * PM))), (unsigned)((g.N + BN - 1) / BN));
+  const dim3 grid((unsigned)(2 * ((g.M + 2 * PM - 1) / (2 * PM))), (unsigned)((g.N + BN - 1) / BN), (unsigned)nb);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(ma, mb, mc, (int)g.M, (int)g.N, (int)g.K,
                                               reinterpret_cast<const __half*>(g.row_scale),
                                               reinterpret_cast<const __half*>(g.col_scale),
                                               reinterpret_cast<const __half*>(g.zero_point), g.row_sum, epi_arg(g), g.c,
-                                              (uint64_t)wait_timeout_ns(), status);
+                                              bt, (uint64_t)wait_timeout_ns(), status);
   return cudaGetLastError();
 }
 

@@ -122,6 +122,24 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int elem, uint64_t row_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_map3(CUtensorMap* map, const void* base, int elem, uint64_t row_elems, uint64_t rows, uint64_t batch,
+                      uint64_t item_stride, uint32_t box_x, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const uint64_t row_bytes = row_elems * (uint64_t)elem;
+  if (batch <= 1) item_stride = (rows * row_bytes + 15) / 16 * 16;   // one item: any valid stride
+  const cuuint64_t dims[3] = {row_elems, rows, batch < 1 ? 1 : batch};
+  const cuuint64_t strides[2] = {row_bytes, item_stride};
+  const cuuint32_t box[3] = {box_x, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = elem == 4   ? CU_TENSOR_MAP_DATA_TYPE_INT32
+                                 : elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int sm_count() {
   static int n[64] = {};
   int dev = 0;

@@ -318,6 +318,48 @@ def test_batched_shared_weights_f16xi4():
                          f16_ulps=1)
 
 
+# shapes the CTA-pair kernel serves (short K, or grids that fill the GPU)
+@pytest.mark.parametrize("bits,M,N,K", [(8, 320, 448, 256), (8, 600, 3840, 2048), (4, 600, 3840, 1024),
+                                        (2, 328, 448, 256)])
+def test_batched_one_grid_every_operand_strided(bits, M, N, K):
+    """Items on the CTA-pair kernel run as one grid (batch = grid z): A, B, both
+    scales and C all per item; int8 x int8 at K = 2048 also exercises the
+    chunked accumulation, whose running high parts live in each item's output."""
+    rng = np.random.default_rng(200 + bits + K)
+    nb = 3
+    A = W.int8_uniform(rng, (nb, M, K))
+    Bq = [_codes(rng, bits, (N, K)) for _ in range(nb)]
+    sw = W.uniform_f16(rng, (nb, N), 1e-3, 1e-2)
+    sx = W.uniform_f16(rng, (nb, M), 1e-3, 1e-1)
+    if bits == 8:
+        Bw = dev(np.stack(Bq))
+        y = host(bq.bq_gemm_i8xi8_batched(dev(A), Bw, row_scale=dev(sx), col_scale=dev(sw)))
+        c = host(bq.bq_gemm_i8xi8_batched(dev(A), Bw))
+    else:
+        Bw = dev(np.stack([O.pack(b, bits, "interleaved") for b in Bq]))
+        fn = bq.bq_gemm_i8xi4_batched if bits == 4 else bq.bq_gemm_i8xi2_batched
+        y = host(fn(dev(A), Bw, "interleaved", row_scale=dev(sx), col_scale=dev(sw)))
+        c = host(fn(dev(A), Bw, "interleaved"))
+    torch.cuda.synchronize()
+    assert bq.bq_device_status(reset=True) == bq.BQ_OK
+    for b in range(nb):
+        c_ref = O.gemm_int(A[b], Bq[b])
+        assert (c[b] == c_ref).all(), f"item {b}"
+        assert (y[b].view(np.uint16) == O.dequant(c_ref, sw[b], sx[b]).view(np.uint16)).all(), f"item {b}"
+
+
+def test_batched_one_grid_f16xi4_per_item():
+    rng = np.random.default_rng(9)
+    nb, M, N, K = 3, 260, 512, 256
+    X = W.normal_f16(rng, (nb, M, K), 1.0)
+    q = [W.int4_uniform(rng, (N, K)) for _ in range(nb)]
+    s = W.uniform_f16(rng, (nb, N), 0.008, 0.016)
+    Wp = dev(np.stack([O.pack(qq, 4, "plain") for qq in q]))
+    y = host(bq.bq_gemm_f16xi4_batched(dev(X), Wp, dev(s), layout="plain"))
+    for b in range(nb):
+        assert_f16_close(y[b], O.gemm_f16xq(X[b], q[b], s[b]), s[b][None, :].astype(np.float64), f"item {b}")
+
+
 def test_activation_none_matches_plain_call():
     rng = np.random.default_rng(11)
     A = W.int8_uniform(rng, (64, 256))
