@@ -315,10 +315,11 @@ def gemm_f16xq(x: np.ndarray, w_codes: np.ndarray, scale: np.ndarray, act: str =
     """Y[i, j] = fp16( act( s[j] * sum_k float(X[i, k]) * q[j, k] ) ).
 
     The sum is a float64 matmul (library step).  For fp16 X and 4-bit codes
-    every product needs at most 15 significant bits and the partial sums of
-    K <= 2**16 terms stay inside float64's 53-bit significand, so the sum is
-    exact; the per-channel scale is applied after it (reading Q11), then the
-    activation (reading Q15).
+    every product is exact (at most 15 significant bits); the sum is exact
+    too while the products' exponents span less than 53 - 15 - log2(K) bits,
+    and otherwise rounds at 2**-53 relative to the largest partial sum, far
+    inside the fp16 tolerance.  The per-channel scale is applied after it
+    (reading Q11), then the activation (reading Q15).
     """
     acc = np.asarray(x, dtype=np.float64) @ np.asarray(w_codes, dtype=np.float64).T
     v = acc * scale.astype(np.float64)[None, :]
