@@ -45,17 +45,22 @@
 // the same SM's tensor memory.
 //
 // Chunked accumulation (DR, int8 x int8 with K > 1024).  A product of two
-// int8 codes reaches 2**14, so one 64-k block adds up to 2**20 and an fp32
-// chain of more than 16 blocks may pass 2**24, where odd integers are no
-// longer representable.  In DR mode the MMA issuer commits the end of every
-// chunk of CH_KB = 15 k-blocks; each consumer warp then reads its part of the
-// accumulator D (exact), splits it as D = 8192 h + L with h = rint(D / 8192),
-// writes L (|L| <= 4096) back into tensor memory and arrives; only then are
-// the next chunk's MMAs issued, on top of L, so every partial sum stays below
-// 4096 + 15 * 2**20 < 2**24.  The high parts h accumulate as integers in the
-// output's own bytes (int16 per element for fp16 outputs, int32 for int32
-// outputs; every element belongs to one thread of one CTA), and the epilogue
-// forms Cint = 8192 * sum(h) + rint(D) exactly before the dequantisation.
+// int8 codes lies in [-128 * 127, 128 * 128], so an fp32 chain longer than
+// 16 k-blocks of 64 may pass 2**24, where odd integers are no longer
+// representable.  In DR mode K is cut into chunks of CH_KB = 16 k-blocks that
+// accumulate alternately into two TMEM accumulators (the int8 activations then
+// go to shared memory as fp16 tiles, like fp16 activations, to leave tensor
+// memory to the accumulators).  When chunk c is done, four drain warps (one
+// per TMEM lane quadrant) read its accumulator D (exact) while chunk c + 1
+// runs in the other one, split it as D = 8192 h + L with h = ceil(D / 8192),
+// write L (-8192 < L <= 0) back and arrive.  Chunk c + 2 accumulates on top
+// of L: its partial sums stay in [-8191 - 1024 * 16256, 1024 * 16384], inside
+// +-2**24, so every value the accumulator takes is an exact integer.  The
+// high parts h add up as integers in the output's own bytes (int16 per
+// element for fp16 outputs, int32 for int32 outputs; every element belongs to
+// one drain thread of one CTA), and the epilogue forms
+// Cint = 8192 * sum(h) + D0 + D1 exactly before the dequantisation.  The
+// splits use full-rate fp32 and integer arithmetic only (split_high, exact_sum).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -73,12 +78,14 @@ constexpr int PK = 64;                   // k per block: one 128-byte fp16 swizz
 constexpr int P_NA = 2;                  // activation converter groups (4 warps each)
 constexpr int P_NA_Q = 4;                // the same, quantising fp16 activations
 constexpr int P_NB_Q = 4;                // weight converter groups beside them
+constexpr int P_NB_DR = 4;               // weight converter groups with chunked accumulation
+constexpr int ST_DR = 4;                 // MMA stages with chunked accumulation (fp16 A and B tiles)
 constexpr int P_NB_I8 = 6;               // weight converter groups, int8 activations
 constexpr int P_NB_F16 = 6;              // weight converter groups, fp16 activations
 constexpr int P_BW = 2;                  // warps per weight converter group
 constexpr int P_B_THREADS = P_BW * 32;   // weight converters per group
 constexpr uint64_t P_DRAIN_NS = 4000000000ull;
-constexpr int CH_KB = 15;                // k-blocks per accumulation chunk (DR mode)
+constexpr int CH_KB = 16;                // k-blocks per accumulation chunk (DR mode)
 constexpr float H_UNIT = 8192.0f;        // weight of one high-part unit (2**13)
 
 // AF16: fp16 activations, loaded by TMA straight into the MMA's 128B-swizzled
@@ -87,15 +94,17 @@ constexpr float H_UNIT = 8192.0f;        // weight of one high-part unit (2**13)
 // int8 activations, converted into tensor memory, one accumulator; with AQ
 // the activations arrive as fp16 and the activation converters quantise them
 // to int8 codes (the row scales given) before storing them the same way.
-template <int BBITS, int BN, int ST, int RST, bool AF16, bool AQ = false>
+template <int BBITS, int BN, int ST, int RST, bool AF16, bool AQ = false, bool DR = false>
 struct PairCfg {
   static constexpr int HB = BN / 2;                            // weight rows per CTA
   // quantising converters (AQ) do several times the work of an int8 conversion: more of them
-  static constexpr int NA = AF16 ? 0 : (AQ ? P_NA_Q : P_NA);  // activation converter groups
+  static constexpr int NA = AF16 ? 0 : ((AQ && !DR) ? P_NA_Q : P_NA);  // activation converter groups
   static constexpr int A_WARPS = 4 * NA;
-  static constexpr int NB = AF16 ? P_NB_F16 : (AQ ? P_NB_Q : P_NB_I8);   // weight converter groups
+  static constexpr int NB = AF16 ? P_NB_F16 : (DR ? P_NB_DR : (AQ ? P_NB_Q : P_NB_I8));   // weight converter groups
   static constexpr int CONSUMER_WARPS = A_WARPS + NB * P_BW;
-  static constexpr int MMA_WARP = CONSUMER_WARPS;
+  // DR: one warp per TMEM lane quadrant drains the chunks in the background
+  static constexpr int DRAIN_WARPS = DR ? 4 : 0;
+  static constexpr int MMA_WARP = CONSUMER_WARPS + DRAIN_WARPS;
   static constexpr int PRODUCER_WARP = MMA_WARP + 1;
   static constexpr int THREADS = (PRODUCER_WARP + 1) * 32;
   // a raw stage holds RKB k-blocks so that every TMA box row is 128 bytes (64
@@ -112,14 +121,15 @@ struct PairCfg {
   static constexpr int A_BOX = PM * 128;                       // int8 activations: 2 k-blocks x 128 rows
   static constexpr int A_KB = PM * 128;                        // fp16 activations: 1 k-block x 128 rows
   static constexpr int A_RAW = AF16 ? 0 : (AQ ? A_KB * RKB : A_BOX * (RKB / 2));
-  static constexpr int A_TILE = AF16 ? PM * 128 : 0;           // fp16 activation tile of one MMA stage
+  static constexpr bool A_SMEM = AF16 || DR;                   // A read by the MMA from shared memory
+  static constexpr int A_TILE = A_SMEM ? PM * 128 : 0;         // fp16 activation tile of one MMA stage
   static constexpr int B_TILE = HB * 128;                      // fp16 weight tile of one MMA stage
   static constexpr int STAGE = A_TILE + B_TILE;
   static constexpr int RSTAGE = (A_RAW + B_RAW + 1023) / 1024 * 1024;
-  static constexpr int NACC = AF16 ? 2 : 1;                    // accumulator slices
+  static constexpr int NACC = (AF16 || DR) ? 2 : 1;            // accumulators (halves of K; DR: chunks in turn)
   static constexpr int A_COLS = PK / 2;                        // TMEM columns of one activation stage
   static constexpr int ACC_COLS = NACC * BN;
-  static constexpr int USED_COLS = ACC_COLS + (AF16 ? 0 : ST * A_COLS);
+  static constexpr int USED_COLS = ACC_COLS + (A_SMEM ? 0 : ST * A_COLS);
   static constexpr int NCOLS = USED_COLS <= 256 ? 256 : 512;
   static constexpr int OFF_RAW = ST * STAGE;
   static constexpr int STG_BYTES = 32 * 32 * 4;                // epilogue staging box per warp (int32)
@@ -144,7 +154,7 @@ struct PairCfg {
   // parity of a phase two behind, which needs n <= ST.
   static_assert(NA <= ST && NB <= ST, "converter groups per stage ring");
   static_assert(CONSUMER_WARPS * STG_BYTES <= OFF_BAR, "epilogue staging fits in the pipeline buffers");
-  static_assert((3 * ST + 2 * RST + 3) * 8 + 4 <= 256, "barrier area");
+  static_assert((3 * ST + 2 * RST + 5) * 8 + 4 <= 256, "barrier area");
 };
 
 // Batched launch (grid z = item): element strides of the scales, the byte
@@ -172,86 +182,122 @@ __device__ __forceinline__ bool out_span_ok(size_t off, int M, int N, int* statu
   return false;
 }
 
-// DR: one consumer warp's drain of chunk boundary b (the accumulator after
-// k-block CH_KB * b - 1).  The warp covers its TMEM lane quadrant (tile rows
-// 32q .. 32q + 31) and its (at most two) 32-column chunks, the same rows and
-// columns it stores in the epilogue: it splits every accumulator value as
-// D = 8192 h + L, writes L back, arrives on the even CTA's drained barrier
-// and then adds h to the running high parts in the output's bytes (int16 for
-// fp16 outputs, int32 for int32 outputs).  False if a wait gave up.
-template <int BN, int PARTS>
-__device__ __forceinline__ bool pair_drain(int b, uint32_t tmem, uint64_t* chunk_bar, uint64_t* drained_bar, int warp,
-                                        int lane, int m0, int n0, int M, int N, int epi, void* out,
-                                        uint64_t timeout_ns, int* status) {
-  const int q = warp & 3, part = warp >> 2;
+// Split of an accumulator value D (an integer, |D| < 2**24) as D = 8192 h + L
+// without conversion instructions, which issue at a quarter of the FMA rate:
+// u = D / 8192 + 1.5 * 2**23, rounded once, lies in [2**23, 2**24) where fp32
+// steps by 1, so u = 1.5 * 2**23 + h with h = rint(D / 8192) (ties to even),
+// and the bit pattern of u is 0x4B400000 + h (|h| < 2**22).
+constexpr uint32_t RNE_MAGIC_BITS = 0x4B400000u;   // bit pattern of 1.5 * 2**23
+__device__ __forceinline__ float split_high(float d) { return __fmaf_rn(d, 1.0f / H_UNIT, RNE_MAGIC); }
+// The same with h = ceil(D / 8192) (the sum rounded toward +infinity), so
+// that L = D - 8192 h lies in (-8192, 0]
+__device__ __forceinline__ float split_high_up(float d) { return __fmaf_ru(d, 1.0f / H_UNIT, RNE_MAGIC); }
+// h as an int32, from u = split_high(D)
+__device__ __forceinline__ int split_h(float u) { return (int)(__float_as_uint(u) - RNE_MAGIC_BITS); }
+// L = D - 8192 h, exact (|L| <= 4096; -8192 < L <= 0 after split_high_up)
+__device__ __forceinline__ float split_low(float d, float u) {
+  return __fmaf_rn(-H_UNIT, __fsub_rn(u, RNE_MAGIC), d);
+}
+
+// D0 + D1 + 8192 hd exactly, for accumulator values D0 and D1 (integers,
+// |D| <= 2**24) and an integer hd: returns the pattern of H + 1.5 * 2**23 for
+// H = h0 + h1 + hd (|H| < 2**22) and sets l = L0 + L1 (exact, |l| <= 8192), so
+// that the sum is 8192 H + l.  Unsigned arithmetic: the two patterns together
+// pass the int32 range before the subtraction brings them back.
+__device__ __forceinline__ int exact_sum(float d0, float d1, int hd, float& l) {
+  const float u0 = split_high(d0), u1 = split_high(d1);
+  l = __fadd_rn(split_low(d0, u0), split_low(d1, u1));
+  return (int)(__float_as_uint(u0) + __float_as_uint(u1) - RNE_MAGIC_BITS + (uint32_t)hd);
+}
+
+// DR: drain warp q's share of chunk c (k-blocks CH_KB c .. CH_KB (c + 1) - 1,
+// accumulated in accumulator c & 1): TMEM lane quadrant q (tile rows
+// 32q .. 32q + 31), every 32-column chunk of the tile.  Each accumulator value
+// is split as D = 8192 h + L, L is written back, and h is added to the running
+// high parts in the output's bytes (int16 for fp16 outputs, int32 for int32
+// outputs; the first drain writes them); then the warp arrives on the even
+// CTA's drained barrier of that accumulator.  If the chunk's barrier wait
+// gives up, the warp still arrives (the MMA issuer then finds the status).
+template <int BN>
+__device__ __forceinline__ void pair_drain(int c, uint32_t tmem, uint64_t* chunk_bar, uint64_t* drained_bar, int q,
+                                           int lane, int m0, int n0, int M, int N, int epi, void* out,
+                                           uint64_t timeout_ns, int* status) {
   const int row0 = m0 + 32 * q, row = row0 + lane;
-  if (!__all_sync(0xffffffffu, mbar_wait(chunk_bar, (uint32_t)((b - 1) & 1), timeout_ns, status))) return false;
+  const int acc = c & 1;
+  const bool ready =
+      __all_sync(0xffffffffu, mbar_wait(&chunk_bar[acc], (uint32_t)((c >> 1) & 1), timeout_ns, status));
   tc_fence_after();
-  uint32_t hp[2][16];   // high parts, two int16 per word
-  bool live[2];
+  // chunks whose columns start inside N, for a quadrant with rows inside M (warp-uniform)
+  int nch = 0;
+  if (ready && row0 < M) {
+    nch = (N - n0 + 31) / 32;
+    if (nch > BN / 32) nch = BN / 32;
+  }
+#pragma unroll 1
+  for (int ch = 0; ch < nch; ++ch) {
+    const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + 32 * ch);
+    const size_t off = (size_t)row * N + n0 + 32 * ch;
+    const bool mine = row < M && out_span_ok(off, M, N, status);
+    // fp16 outputs: the running high parts (int16) of this row's 32 columns
+    // are loaded first, so that their latency overlaps the tensor-memory work
+    uint32_t old[16];
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int ch = part + j * PARTS;
-    live[j] = ch < BN / 32 && n0 + 32 * ch < N && row0 < M;   // warp-uniform
-    if (live[j]) {
-      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * ch);
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(ta, r);
-      tmem_ld_wait_tied(r);
+    for (int i = 0; i < 16; ++i) old[i] = 0;
+    if (mine && c > 0 && epi != EPI_I32) {
+      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(out) + off);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        // D = 8192 h + L exactly: D is an integer below 2**24, h = rint(D / 8192), |L| <= 4096
-        const float f0 = __uint_as_float(r[2 * i]), f1 = __uint_as_float(r[2 * i + 1]);
-        const float h0 = rintf(f0 * (1.0f / H_UNIT)), h1 = rintf(f1 * (1.0f / H_UNIT));
-        r[2 * i] = __float_as_uint(fmaf(-H_UNIT, h0, f0));
-        r[2 * i + 1] = __float_as_uint(fmaf(-H_UNIT, h1, f1));
-        hp[j][i] = ((uint32_t)(int)h0 & 0xffffu) | ((uint32_t)(int)h1 << 16);
+      for (int v = 0; v < 4; ++v) {
+        const uint4 o = p[v];
+        old[4 * v] = o.x;
+        old[4 * v + 1] = o.y;
+        old[4 * v + 2] = o.z;
+        old[4 * v + 3] = o.w;
       }
-      tmem_st_32x32b_x32(ta, r);
-      tmem_st_wait_tied(r);
+    }
+    uint32_t r[32];
+    uint32_t hp[16];   // high parts, two int16 per word
+    tmem_ld_32x32b_x32(ta, r);
+    tmem_ld_wait_tied(r);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      // D = 8192 h + L exactly, with h = ceil(D / 8192) and -8192 < L <= 0, in
+      // full-rate arithmetic only (no conversion instructions): see split_high
+      const float f0 = __uint_as_float(r[2 * i]), f1 = __uint_as_float(r[2 * i + 1]);
+      const float u0 = split_high_up(f0), u1 = split_high_up(f1);
+      r[2 * i] = __float_as_uint(split_low(f0, u0));
+      r[2 * i + 1] = __float_as_uint(split_low(f1, u1));
+      // the low 16 bits of u's pattern are h modulo 2**16
+      hp[i] = __vadd2(__byte_perm(__float_as_uint(u0), __float_as_uint(u1), 0x5410), old[i]);
+    }
+    tmem_st_32x32b_x32(ta, r);
+    tmem_st_wait_tied(r);
+    if (mine) {
+      if (epi == EPI_I32) {   // int32 running sums (they may pass the int16 range at long K)
+        int4* p = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + off);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint32_t w0 = hp[2 * v], w1 = hp[2 * v + 1];
+          int4 h = make_int4((int)(int16_t)(w0 & 0xffffu), (int)w0 >> 16, (int)(int16_t)(w1 & 0xffffu),
+                             (int)w1 >> 16);
+          if (c > 0) {
+            const int4 o = p[v];
+            h.x += o.x;
+            h.y += o.y;
+            h.z += o.z;
+            h.w += o.w;
+          }
+          p[v] = h;
+        }
+      } else {
+        uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + off);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) p[v] = make_uint4(hp[4 * v], hp[4 * v + 1], hp[4 * v + 2], hp[4 * v + 3]);
+      }
     }
   }
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(drained_bar), 0));
-  if (row >= M) return true;
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    if (!live[j]) continue;
-    const size_t off = (size_t)row * N + n0 + 32 * (part + j * PARTS);
-    if (!out_span_ok(off, M, N, status)) continue;
-    if (epi == EPI_I32) {
-      int4* p = reinterpret_cast<int4*>(static_cast<int32_t*>(out) + off);
-#pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const uint32_t w0 = hp[j][2 * v], w1 = hp[j][2 * v + 1];
-        int4 h = make_int4((int)(int16_t)(w0 & 0xffffu), (int)w0 >> 16, (int)(int16_t)(w1 & 0xffffu), (int)w1 >> 16);
-        if (b > 1) {
-          const int4 o = p[v];
-          h.x += o.x;
-          h.y += o.y;
-          h.z += o.z;
-          h.w += o.w;
-        }
-        p[v] = h;
-      }
-    } else {
-      uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + off);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uint4 h = make_uint4(hp[j][4 * v], hp[j][4 * v + 1], hp[j][4 * v + 2], hp[j][4 * v + 3]);
-        if (b > 1) {
-          const uint4 o = p[v];
-          h.x = __vadd2(h.x, o.x);
-          h.y = __vadd2(h.y, o.y);
-          h.z = __vadd2(h.z, o.z);
-          h.w = __vadd2(h.w, o.w);
-        }
-        p[v] = h;
-      }
-    }
-  }
-  return true;
+  if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&drained_bar[acc]), 0));
 }
 
 // ACTV: the fp16 epilogue applies the activation in bits 4.. of `epi` (a
@@ -261,17 +307,15 @@ __device__ __forceinline__ bool pair_drain(int b, uint32_t tmem, uint64_t* chunk
 // ZP (fp16 activations): unsigned 4-bit weight codes with a per-column zero
 // point; the epilogue adds (8 - zero_point[j]) * row_sum[i].
 template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool AQ, bool ACTV, bool DR, bool ZP>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST, AF16, AQ>::THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, ST, RST, AF16, AQ, DR>::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_c, int M, int N, int K,
                      const __half* __restrict__ row_scale, const __half* __restrict__ col_scale,
                      const __half* __restrict__ zero_point, const float* __restrict__ row_sum, int epi,
                      void* out, const PairBatch bt, uint64_t timeout_ns, int* status) {
-  using C = PairCfg<BBITS, BN, ST, RST, AF16, AQ>;
+  using C = PairCfg<BBITS, BN, ST, RST, AF16, AQ, DR>;
   static_assert(!DR || (BBITS == 8 && !AF16), "chunked accumulation is for int8 x int8");
   static_assert(!ZP || (AF16 && BBITS == 4), "zero points are for fp16 x 4-bit");
-  // DR: each consumer warp drains at most two 32-column chunks of its quadrant
-  static_assert(!DR || BN / 32 <= 2 * (C::CONSUMER_WARPS / 4), "drain chunks per warp");
   const int actfn = epi >> 4;
   epi &= 15;
   extern __shared__ uint8_t smem_raw[];
@@ -283,9 +327,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
   uint64_t* rempty_bar = rfull_bar + RST;                                // raw stage read
   uint64_t* accum_bar = rempty_bar + RST;                                // all MMAs done
   uint64_t* afull_bar = accum_bar + 1;                                   // fp16 activation tile landed
-  uint64_t* chunk_bar = afull_bar + ST;                                  // DR: MMAs of a chunk done
-  uint64_t* drained_bar = chunk_bar + 1;                                 // DR (even CTA): chunk drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained_bar + 1);
+  uint64_t* chunk_bar = afull_bar + ST;                                  // DR: MMAs of a chunk done (per accumulator)
+  uint64_t* drained_bar = chunk_bar + 2;                                 // DR (even CTA): chunk drained (per accumulator)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained_bar + 2);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -300,7 +344,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
   const int n0 = blockIdx.y * BN;                                      // the pair's output columns
   const int nb0 = n0 + (int)rank * C::HB;                              // this CTA's weight rows
   const int nkb = K / PK;
-  const int ndr = DR ? (nkb - 1) / CH_KB : 0;   // chunk boundaries inside K (DR)
+  // DR: chunks of CH_KB k-blocks; chunk c is drained when chunk c + 2 will reuse its accumulator
+  const int nchunks = DR ? (nkb + CH_KB - 1) / CH_KB : 1;
+  const int ndrain = nchunks > 2 ? nchunks - 2 : 0;
   const uint32_t rzero = (uint32_t)K >> 30;      // 0 (K <= 65536), not known to the compiler
 
   if (tid == 0) {
@@ -314,8 +360,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       mbar_init(&rempty_bar[s], C::RAW_READERS);   // every group that reads a raw stage releases it once
     }
     mbar_init(accum_bar, 1);
-    mbar_init(chunk_bar, 1);
-    mbar_init(drained_bar, 2 * C::CONSUMER_WARPS);   // one arrival per consumer warp of each CTA
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&chunk_bar[i], 1);
+      // one arrival per drain warp of each CTA (a count of 0 is not a valid
+      // mbarrier; without DR the barrier is unused)
+      mbar_init(&drained_bar[i], C::DRAIN_WARPS > 0 ? 2 * C::DRAIN_WARPS : 1);
+    }
     mbar_fence_init();
   }
   if (warp == C::MMA_WARP) {
@@ -334,23 +384,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
   cluster_sync_all();
 
   bool ok = true;
-  int db = 1;   // DR: next chunk boundary this warp drains
-  // DR: before a consumer writes the stage of k-block kb, it drains every
-  // boundary that the MMAs of kb - ST (the stage's previous use) lie behind.
-  // By then it has converted all of its k-blocks of the drained chunk, so the
-  // chunk's MMAs never wait for it, and the ST stages after a boundary are
-  // already converted when the MMAs resume.
-  auto drain_before = [&](int kb) -> bool {
-    if constexpr (DR) {
-      while (db <= ndr && kb >= db * CH_KB + ST) {
-        if (!pair_drain<BN, C::CONSUMER_WARPS / 4>(db, tmem, chunk_bar, drained_bar, warp, lane, m0, n0, M, N, epi,
-                                                   out, timeout_ns, status))
-          return false;
-        ++db;
-      }
-    }
-    return true;
-  };
+  // DR: the drain warps and the consumer warps meet here before the epilogue
+  // reads the high parts the drains stored
+  constexpr int DRAIN_SYNC_THREADS = (C::CONSUMER_WARPS + C::DRAIN_WARPS) * 32;
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -402,19 +438,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       const int kb_half = C::NACC == 2 ? (nkb + 1) / 2 : nkb;
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % ST;
-        if (DR && kb > 0 && kb % CH_KB == 0) {
-          // the next chunk adds on top of the drained accumulator (both CTAs' consumer warps)
-          const int b = kb / CH_KB;
-          if (!__all_sync(0xffffffffu, mbar_wait_cluster(drained_bar, (b - 1) & 1, timeout_ns, status))) break;
+        const int chunk = kb / CH_KB;
+        if (DR && kb % CH_KB == 0 && chunk >= 2) {
+          // chunk c adds on top of what the drain of chunk c - 2 left in the same accumulator
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait_cluster(&drained_bar[chunk & 1], ((chunk - 2) >> 1) & 1, timeout_ns, status)))
+            break;
         }
         if (!__all_sync(0xffffffffu, mbar_wait_cluster(&full_bar[s], (kb / ST) & 1, timeout_ns, status))) break;
         tc_fence_after();
-        const int slice = kb < kb_half ? 0 : 1;
-        const bool first = kb == 0 || kb == kb_half;
+        // DR: accumulator chunk & 1, fresh for chunks 0 and 1; otherwise slices of halves of K
+        const int slice = DR ? (chunk & 1) : (kb < kb_half ? 0 : 1);
+        const bool first = DR ? (kb % CH_KB == 0 && chunk < 2) : (kb == 0 || kb == kb_half);
         const uint32_t d = tm + (uint32_t)(slice * BN);
         const uint64_t bdesc = smem_desc_sw128(smem_base + s * C::STAGE + C::A_TILE);
         if (elect_one()) {
-          if constexpr (AF16) {
+          if constexpr (C::A_SMEM) {
             const uint64_t adesc = smem_desc_sw128(smem_base + s * C::STAGE);
 #pragma unroll
             for (int kk = 0; kk < PK / 16; ++kk)   // +32 bytes along K = +2 in the address field
@@ -426,8 +465,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
               tc_mma_f16_ts_pair(d, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
           }
           tc_commit_pair(&empty_bar[s], 0x3);
-          // DR: the last k-block of a chunk (with more to come): let the consumers drain
-          if (DR && (kb + 1) % CH_KB == 0 && kb + 1 < nkb) tc_commit_pair(chunk_bar, 0x3);
+          // DR: the last k-block of a chunk whose accumulator a later chunk reuses: let the consumers drain it
+          if (DR && (kb + 1) % CH_KB == 0 && chunk < ndrain) tc_commit_pair(&chunk_bar[chunk & 1], 0x3);
         }
         __syncwarp();
       }
@@ -445,10 +484,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
     RowQuant rq{};
     if constexpr (AQ) rq = row_quant(m0 + r < M ? __half2float(row_scale[m0 + r]) : 0.0f);
     for (int kb = warp >> 2; kb < nkb; kb += C::NA) {
-      if (!drain_before(kb)) {
-        ok = false;
-        break;
-      }
       const int grp = kb / C::RKB, rs = grp % RST;
       // the group's first k-block of a raw stage waits for it to land
       if (kb % C::RKB < C::NA && !warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
@@ -490,25 +525,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         ok = false;
         break;
       }
-      // order the store after the MMAs whose completion the barrier reported:
-      // without the fence it may overwrite the stage while they still read it
-      tc_fence_after();
-      tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::ACC_COLS + s * C::A_COLS), h);
-      tmem_st_wait_tied(h);
-      tc_fence_before();
+      if constexpr (C::A_SMEM) {
+        // DR: the row's 64 fp16 values into the stage's 128B-swizzled K-major tile
+        uint8_t* ta = smem + s * C::STAGE;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) st_chunk(ta, r, j, make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]));
+        fence_proxy_async_smem();   // generic stores -> visible to the tensor core (async proxy)
+      } else {
+        // order the store after the MMAs whose completion the barrier reported:
+        // without the fence it may overwrite the stage while they still read it
+        tc_fence_after();
+        tmem_st_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::ACC_COLS + s * C::A_COLS), h);
+        tmem_st_wait_tied(h);
+        tc_fence_before();
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&full_bar[s]), 0));
     }
-  } else {
+  } else if (warp < C::CONSUMER_WARPS) {
     // ------------------------------------------------------------ weights -> fp16 smem
     // B group g (warps A_WARPS + g * P_BW ..) converts the k-blocks kb = g (mod NB)
     const int bw = warp - C::A_WARPS;
     const int c = (bw % P_BW) * 32 + lane;                // converter thread within its group
     for (int kb = bw / P_BW; kb < nkb; kb += C::NB) {
-      if (!drain_before(kb)) {
-        ok = false;
-        break;
-      }
       const int grp = kb / C::RKB, rs = grp % RST;
       if (kb % C::RKB < C::NB && !warp_wait(&rfull_bar[rs], (grp / RST) & 1, timeout_ns, status)) {
         ok = false;
@@ -553,20 +592,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&full_bar[s]), 0));
     }
+  } else if constexpr (DR) {
+    // ------------------------------------------------------------ drain warps (DR)
+    // warp CONSUMER_WARPS + q owns TMEM lane quadrant q; chunk c is drained
+    // while chunk c + 1 is multiplied, before chunk c + 2 reuses the accumulator
+    const int q = warp & 3;
+#pragma unroll 1
+    for (int c = 0; c < ndrain; ++c)
+      pair_drain<BN>(c, tmem, chunk_bar, drained_bar, q, lane, m0, n0, M, N, epi, out, timeout_ns, status);
+    __threadfence_block();   // the high parts' stores, before the consumers read them
+    asm volatile("bar.sync 1, %0;" ::"n"(DRAIN_SYNC_THREADS) : "memory");
   }
 
   // ------------------------------------------------------------ epilogue (consumer warps)
   if (warp < C::CONSUMER_WARPS) {
-    if constexpr (DR) {
-      // boundaries no k-block of this warp lay behind
-      while (ok && db <= ndr) {
-        ok = pair_drain<BN, C::CONSUMER_WARPS / 4>(db, tmem, chunk_bar, drained_bar, warp, lane, m0, n0, M, N, epi,
-                                                   out, timeout_ns, status);
-        ++db;
-      }
-    }
     const bool acc_ok = warp_wait(accum_bar, 0, ok ? timeout_ns : 0, status);
     tc_fence_after();
+    // DR: every consumer thread waits for every drain warp's high parts (exactly once, whatever happened)
+    if constexpr (DR) asm volatile("bar.sync 1, %0;" ::"n"(DRAIN_SYNC_THREADS) : "memory");
     if (acc_ok) {
       // CONSUMER_WARPS / 4 warps share each TMEM lane quadrant; each takes
       // every such 32-column chunk.  The pipeline buffers are idle now: each
@@ -587,7 +630,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, r);
         tmem_ld_wait_tied(r);
-        if constexpr (C::NACC == 2) {
+        if constexpr (C::NACC == 2 && !DR) {
           uint32_t r2[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(col + BN), r2);
           tmem_ld_wait_tied(r2);
@@ -604,40 +647,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
           }
         }
-        // exact integer sums: rint(D), plus 8192 times the drained high parts (DR)
-        int ci[32];
+        // exact integer sums, in r as int32 patterns for int32 outputs: rint(D0);
+        // DR: D0 + D1 + 8192 times the drained high parts (for fp16 outputs that
+        // sum rounded once to fp32, in r as a float)
+        if constexpr (!DR) {
+          if (epi == EPI_I32) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ci[i] = __float2int_rn(__uint_as_float(r[i]));
-        if constexpr (DR) {
+            for (int i = 0; i < 32; ++i) r[i] = (uint32_t)__float2int_rn(__uint_as_float(r[i]));
+          }
+        } else {
           const size_t off = (size_t)row * N + ncol;
-          if (row < M && out_span_ok(off, M, N, status)) {
-            if (epi == EPI_I32) {
-              const int4* p = reinterpret_cast<const int4*>(static_cast<const int32_t*>(out) + off);
+          const bool with_h = ndrain > 0 && row < M && out_span_ok(off, M, N, status);
+          // D1 in two halves of 16 columns (fewer live registers)
 #pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                const int4 h = p[v];
-                ci[4 * v] += h.x * (int)H_UNIT;
-                ci[4 * v + 1] += h.y * (int)H_UNIT;
-                ci[4 * v + 2] += h.z * (int)H_UNIT;
-                ci[4 * v + 3] += h.w * (int)H_UNIT;
-              }
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t r2[16];
+            if (nchunks >= 2) {
+              tmem_ld_32x32b_x16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(col + BN + 16 * hf), r2);
+              tmem_ld_wait_tied(r2);
             } else {
-              const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(out) + off);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) r2[j] = 0u;
+            }
+            if (epi == EPI_I32) {
+              const int4* p = reinterpret_cast<const int4*>(static_cast<const int32_t*>(out) + off) + 4 * hf;
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
-                const uint4 h = p[v];
-                const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+                const int4 h = with_h ? p[v] : make_int4(0, 0, 0, 0);
+                const int hd[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  ci[8 * v + 2 * e] += (int)(int16_t)(w[e] & 0xffffu) * (int)H_UNIT;
-                  ci[8 * v + 2 * e + 1] += ((int)w[e] >> 16) * (int)H_UNIT;
+                  const int j = 4 * v + e, i = 16 * hf + j;
+                  float l;
+                  const int hm = exact_sum(__uint_as_float(r[i]), __uint_as_float(r2[j]), hd[e], l);
+                  r[i] = (uint32_t)((hm - (int)RNE_MAGIC_BITS) * (int)H_UNIT + split_h(__fadd_rn(l, RNE_MAGIC)));
+                }
+              }
+            } else {
+              const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(out) + off) + 2 * hf;
+#pragma unroll
+              for (int v = 0; v < 2; ++v) {
+                const uint4 h = with_h ? p[v] : make_uint4(0, 0, 0, 0);
+                const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int j = 8 * v + e, i = 16 * hf + j;
+                  const int hd = (e & 1) ? ((int)w[e >> 1] >> 16) : (int)(int16_t)(w[e >> 1] & 0xffffu);
+                  float l;
+                  const int hm = exact_sum(__uint_as_float(r[i]), __uint_as_float(r2[j]), hd, l);
+                  // 8192 H + L rounded once (H: its pattern less that of 1.5 * 2**23)
+                  r[i] = __float_as_uint(__fmaf_rn(H_UNIT, __fsub_rn(__int_as_float(hm), RNE_MAGIC), l));
                 }
               }
             }
           }
-          // the fp16 dequantisation starts from the exact sum (one rounding to fp32)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__int2float_rn(ci[i]));
         }
         if (lane == 0) bulk_wait_read_all();   // the previous box has left the staging buffer
         __syncwarp();
@@ -646,7 +709,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             *reinterpret_cast<int4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                make_int4(ci[4 * j], ci[4 * j + 1], ci[4 * j + 2], ci[4 * j + 3]);
+                make_int4((int)r[4 * j], (int)r[4 * j + 1], (int)r[4 * j + 2], (int)r[4 * j + 3]);
         } else {
           uint32_t hv[16];
 #pragma unroll
@@ -682,7 +745,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
           bulk_commit_group();
         }
       }
-      if (lane == 0) bulk_wait_all();
+      // the staging buffers must outlive the TMA engine's reads of them; the
+      // global writes themselves are complete when the grid is
+      if (lane == 0) bulk_wait_read_all();
       __syncwarp();
     }
   }
@@ -702,7 +767,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
 // ---------------------------------------------------------------------------
 template <int BBITS, int BN, bool INTER, int ST, int RST, bool AF16, bool AQ, bool ACTV, bool DR, bool ZP = false>
 cudaError_t launch_pair_t(const GemmArgs& g, cudaStream_t stream) {
-  using C = PairCfg<BBITS, BN, ST, RST, AF16, AQ>;
+  using C = PairCfg<BBITS, BN, ST, RST, AF16, AQ, DR>;
   int* status = nullptr;
   cudaError_t e = device_status_ptr(&status);
   if (e != cudaSuccess) return e;
@@ -750,7 +815,8 @@ template <int BBITS, int BN, int ST, int RST, bool AF16, bool AQ, bool ACTV>
 cudaError_t launch_pair_act(const GemmArgs& g, cudaStream_t stream) {
   if constexpr (BBITS == 8 && !AF16) {
     // int8 x int8 beyond 16 k-blocks: chunked accumulation keeps the sums exact
-    if (g.K > 16 * PK) return launch_pair_t<8, BN, true, ST, RST, false, AQ, ACTV, true>(g, stream);
+    // (fp16 A and B tiles in ST_DR stages, four drain warps; fp16 activations to quantise need wider raw stages)
+    if (g.K > 16 * PK) return launch_pair_t<8, BN, true, ST_DR, AQ ? 2 : 3, false, AQ, ACTV, true>(g, stream);
     return launch_pair_t<8, BN, true, ST, RST, false, AQ, ACTV, false>(g, stream);
   } else if constexpr (AF16) {
     if (g.zero_point) {

@@ -128,6 +128,37 @@ def test_i8xi8_cancellation_activation():
     assert err_over_tol(y[rows], y_ref, s_ij) <= 1.0
 
 
+def test_i8xi8_chunk_extremes_exact():
+    """Chunked accumulation at the edges of its range (CTA pairs, K = 4416:
+    chunks of 16, 16, 16, 16 and 5 k-blocks).  Even rows x even columns are
+    all (-128)(-128), so every full chunk sums to exactly 2**24.  Odd rows x
+    odd columns: the first two chunks sum to 1, which leaves the lowest
+    remainder L = -8191, and every later chunk adds 1024 products -128 * 127
+    on top of it (-16654335 at its end)."""
+    M, N, K = 600, 8192, 4416
+    A = np.zeros((M, K), np.int8)
+    B = np.zeros((N, K), np.int8)
+    A[0::2] = -128
+    B[0::2] = -128
+    A[1::2, 0] = 1
+    A[1::2, 1024] = 1
+    A[1::2, 2048:] = -128
+    B[1::2, 0] = 1
+    B[1::2, 1024] = 1
+    B[1::2, 2048:] = 127
+    rows = np.r_[0, 1, 2, 3, M - 2, M - 1]
+    c_ref = O.gemm_int(A[rows], B)
+    assert c_ref[0, 0] == K * 16384 and c_ref[1, 1] == 2 - (K - 2048) * 16256
+    Ad, Bd = dev(A), dev(B)
+    c = host(bq.bq_gemm_i8xi8(Ad, Bd))
+    assert (c[rows] == c_ref).all(), describe_mismatch(c[rows], c_ref, rows)
+    sw = W.uniform_f16(np.random.default_rng(7), (N,), 1e-3, 1e-2)
+    y = host(bq.bq_gemm_i8xi8(Ad, Bd, col_scale=dev(sw)))
+    r = err_over_tol(y[rows], O.dequant(c_ref, sw), sw[None, :].astype(np.float64))
+    assert r <= 1.0, f"fp16 epilogue err/tol {r:.3g}"
+    assert bq.bq_device_status(reset=True) == bq.BQ_OK
+
+
 def test_i8xi8_int32_long_k_exact():
     """int32 output with K = 16384 (CTA pairs, 17 chunk boundaries): every
     product is (-128)(-128) or 127(-128), so |C| reaches 2**28."""
