@@ -628,6 +628,11 @@ def _profile_workloads():
             wq, sw = bq.bq_quantize_sym(torch.from_numpy(d["W"]).to(dev), 8)
             X = torch.from_numpy(d["X"]).to(dev)
             return lambda: bq.bq_quantized_linear(X, wq, 8, sw)
+        if name == "i8xi8_1024":
+            d = W.cfg1()
+            xq, sx = bq.bq_quantize_sym(torch.from_numpy(d["X"]).to(dev), 8)
+            wq, sw = bq.bq_quantize_sym(torch.from_numpy(d["W"]).to(dev), 8)
+            return lambda: bq.bq_gemm_i8xi8(xq, wq, row_scale=sx, col_scale=sw)
         if name == "pair_i8xi4_4096":
             d = W.cfg2()
             A = torch.from_numpy(d["A"]).to(dev)
@@ -638,7 +643,7 @@ def _profile_workloads():
     return setup
 
 
-PROFILES = ("gemv_m1", "f16xi4_m64", "quantize_4096", "linear_w8_1024", "zp_m1024", "pair_i8xi4_4096")
+PROFILES = ("gemv_m1", "f16xi4_m64", "quantize_4096", "linear_w8_1024", "zp_m1024", "pair_i8xi4_4096", "i8xi8_1024")
 
 
 def run_profile(name, launches=3):

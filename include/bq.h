@@ -143,11 +143,14 @@ bq_status bq_pack_weights(const int8_t* q, int64_t n, int64_t k, int bits, int l
  *   The tensor cores multiply exact fp16 images of the codes into fp32
  *   accumulators, which hold integers exactly up to 2**24: every fp32 chain
  *   is kept within that bound, so the fp16 epilogue starts from the exact
- *   Cint as well.  int8 x int8 products reach 2**14, so its chains are at
- *   most 1024 k long: CTA pairs drain the accumulator every 15 k-blocks
- *   (its high part collects as an integer in the output's own bytes before
- *   the epilogue overwrites them), the single-CTA kernel uses separate TMEM
- *   slices or split-K ranges of at most 16 k-blocks summed as integers.
+ *   Cint as well.  int8 x int8 products reach 2**14, so its fresh chains
+ *   are at most 1024 k long: CTA pairs cut K into chunks of 16 k-blocks and
+ *   drain each finished chunk's accumulator while the next chunk runs (its
+ *   high part collects as an integer in the output's own bytes before the
+ *   epilogue overwrites them; the remainder, in (-8192, 0], stays in the
+ *   accumulator under the chunk after next), the single-CTA kernel uses
+ *   separate TMEM slices or split-K ranges of at most 16 k-blocks summed as
+ *   integers.
  *   Any M >= 0.  Dispatch: M <= 16 runs the skinny kernel (one pass over the
  *   weights; int8 x int8 uses an exact dp4a kernel there), larger M the
  *   tensor-core GEMM: 256-row tiles on CTA pairs when the grid fills the GPU,
