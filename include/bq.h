@@ -314,7 +314,8 @@ bq_status bq_quantized_linear(const uint16_t* X, int64_t M, int64_t K, const voi
  *   Wp         device packed unsigned 4-bit codes, N x K / 2 bytes
  *   col_scale, zero_point  device fp16, N
  *   row_sum    device fp32, M: OUTPUT, row_sum[i] = sum_k X[i, k] in fp32
- *              (a fixed order), used by the epilogue
+ *              (a fixed order), used by the epilogue (M <= 16: formed inside
+ *              the skinny kernel, no extra launch)
  *   Y          device fp16, M x N: OUTPUT
  *   Limits: K % 64 == 0, N % 64 == 0, K <= 65536.  Dispatch as bq_gemm_f16xi4
  *   (M <= 16 the skinny kernel while 16 staged weight rows fit in 64 KB,

@@ -368,7 +368,10 @@ bq_status bq_gemm_f16xu4_zp(const uint16_t* X, const uint8_t* Wp, int layout, in
   if (!aligned16(row_sum) || (zero_point && !aligned16(zero_point))) return BQ_ERR_ALIGNMENT;
   if (K > 0 && !X) return BQ_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_row_sum_f16(X, M, K, row_sum, s) != cudaSuccess) return BQ_ERR_CUDA;
+  // the skinny kernel (the route run_gemm takes for these shapes) forms the
+  // row sums itself and writes them; every other route reads them
+  const bool sums_in_gemv = N > 0 && K > 0 && M <= SKINNY_M && gemv_zp_fits(M, K);
+  if (!sums_in_gemv && launch_row_sum_f16(X, M, K, row_sum, s) != cudaSuccess) return BQ_ERR_CUDA;
   if (N == 0) return BQ_OK;
   GemmArgs g{X, Wp, ACT_F16, 4, layout, M, N, K, nullptr, col_scale, EPI_F16_COL, Y, activation};
   g.zero_point = zero_point;

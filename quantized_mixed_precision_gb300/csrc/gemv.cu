@@ -292,13 +292,18 @@ __device__ __forceinline__ uint4 load_x8(const uint8_t* xr, int k0, bool live) {
 // re-reading the same few L2 lines at each step.
 // ZP (fp16 x 4-bit): unsigned weight codes with a per-column zero point; the
 // epilogue adds (8 - zero_point[n]) * row_sum[m] before the column scale.
+// Every block forms the row sums itself: beside each product MMA, one with an
+// all-ones A fragment sums the same activation fragment over k into fp32
+// (every row of that accumulator holds the sums); the block adds the warps'
+// shares in warp order, the same in every block, and block 0 also writes
+// them to row_sum.
 template <int BBITS, int ACT, int NB, bool INTER, bool FULL, bool XS, bool ZP = false>
 __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* __restrict__ act,
                                                                     const uint8_t* __restrict__ w, int M, int N, int K,
                                                                     const __half* __restrict__ row_scale,
                                                                     const __half* __restrict__ col_scale,
                                                                     const __half* __restrict__ zero_point,
-                                                                    const float* __restrict__ row_sum, int epi,
+                                                                    float* __restrict__ row_sum, int epi,
                                                                     void* __restrict__ out, uint64_t timeout_ns,
                                                                     int* status) {
   static_assert(!ZP || (BBITS == 4 && ACT == ACT_F16), "zero points are for fp16 x 4-bit");
@@ -306,6 +311,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
   const int actfn = epi >> 4;
   epi &= 15;
   __shared__ float red[GEMV_WARPS][NB][4][32];
+  __shared__ float rs_part[ZP ? GEMV_WARPS : 1][ZP ? NB * 8 : 1];   // ZP: the warps' shares of the row sums
   __shared__ __align__(8) uint64_t wbar[GEMV_WARPS];
   __shared__ __align__(8) uint64_t xbar[GEMV_WARPS];
   extern __shared__ __align__(16) uint8_t wsm[];         // 16 staged weight rows, then (XS) the activations
@@ -388,12 +394,19 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
     for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
       for (int i = 0; i < 4; ++i) d[a][nb][i] = 0.0f;
+  float dz[ZP ? NB : 1][4];   // ZP: sums of the activations over this warp's k
+#pragma unroll
+  for (int nb = 0; nb < (ZP ? NB : 1); ++nb)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dz[nb][i] = 0.0f;
+  constexpr uint32_t ONES = 0x3C003C00u;   // two fp16 ones
 
 #pragma unroll 2
   for (int s = s_begin; s < s_stop; ++s) {
     const int kbase = s * C::STEP + t * C::E16;          // first k of this thread's 16 bytes
     // a ragged last step: threads past K read zero weights and activations
-    // of the warp's own first step (staged, finite)
+    // of the warp's own first step (staged, finite); ZP: zero activations,
+    // which the row sums also take
     const bool kin = FULL || kbase < K;
     const int kx = kin ? kbase : s_begin * C::STEP;
     // activation fragments first, overlapping the conversion
@@ -401,7 +414,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
 #pragma unroll
     for (int j = 0; j < C::CPT; ++j)
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = load_x8<ACT, XS>(xr[nb], kx + 8 * j, xv[nb]);
+      for (int nb = 0; nb < NB; ++nb) xb[j][nb] = load_x8<ACT, XS>(xr[nb], kx + 8 * j, xv[nb] && (!ZP || kin));
     const uint32_t woff = (uint32_t)s * STEP_W;
     uint4 va = *reinterpret_cast<const uint4*>(wr0 + (kin ? woff : 0));
     uint4 vb = *reinterpret_cast<const uint4*>(wr1 + (kin ? woff : 0));
@@ -424,16 +437,38 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
           float (&dd)[4] = d[i & 1][nb];
           mma_16816(dd, ha[4 * c + 0], hb[4 * c + 0], ha[4 * c + 1], hb[4 * c + 1], xb[j][nb].x, xb[j][nb].y);
           mma_16816(dd, ha[4 * c + 2], hb[4 * c + 2], ha[4 * c + 3], hb[4 * c + 3], xb[j][nb].z, xb[j][nb].w);
+          if constexpr (ZP) {
+            mma_16816(dz[nb], ONES, ONES, ONES, ONES, xb[j][nb].x, xb[j][nb].y);
+            mma_16816(dz[nb], ONES, ONES, ONES, ONES, xb[j][nb].z, xb[j][nb].w);
+          }
         }
       }
     }
   }
 
+  if constexpr (ZP) {
+    // accumulator row g = 0 (lanes 0..3): columns m = 8 nb + 2 t and 8 nb + 2 t + 1
+    if (g == 0) {
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        rs_part[warp][nb * 8 + 2 * t] = dz[nb][0];
+        rs_part[warp][nb * 8 + 2 * t + 1] = dz[nb][1];
+      }
+    }
+  }
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
     for (int i = 0; i < 4; ++i) red[warp][nb][i][lane] = d[0][nb][i] + d[1][nb][i];
   const bool ok = __syncthreads_and(w_ok ? 1 : 0) != 0;
+  if constexpr (ZP) {
+    if (blockIdx.x == 0 && (int)threadIdx.x < M) {
+      float r = 0.0f;
+#pragma unroll
+      for (int ww = 0; ww < GEMV_WARPS; ++ww) r = __fadd_rn(r, rs_part[ww][threadIdx.x]);
+      row_sum[threadIdx.x] = r;
+    }
+  }
   if (warp < NB && ok) {
     const int nb = warp;
 #pragma unroll
@@ -448,7 +483,12 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) gemv_bulk_kernel(const void* 
       if (epi == EPI_I32) {
         static_cast<int32_t*>(out)[o] = __float2int_rn(acc);
       } else {
-        if constexpr (ZP) acc = __fmaf_rn(__fsub_rn(8.0f, __half2float(zero_point[n])), row_sum[m], acc);
+        if constexpr (ZP) {
+          float r = 0.0f;
+#pragma unroll
+          for (int ww = 0; ww < GEMV_WARPS; ++ww) r = __fadd_rn(r, rs_part[ww][m]);
+          acc = __fmaf_rn(__fsub_rn(8.0f, __half2float(zero_point[n])), r, acc);
+        }
         float v = __fmul_rn(acc, __half2float(col_scale[n]));
         if (epi == EPI_F16_ROWCOL) v = __fmul_rn(v, __half2float(row_scale[m]));
         v = apply_act(v, actfn);
@@ -488,7 +528,7 @@ cudaError_t launch_bulk(const GemmArgs& g, cudaStream_t stream) {
   void* c = g.c;
   uint64_t to = (uint64_t)wait_timeout_ns();
   const __half* zp = reinterpret_cast<const __half*>(g.zero_point);
-  const float* rsum = g.row_sum;
+  float* rsum = const_cast<float*>(g.row_sum);   // ZP: written by block 0
   e = cudaLaunchKernelEx(&cfg, kern, a, b, M, N, K, rsc, csc, zp, rsum, epi, c, to, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -512,6 +552,12 @@ cudaError_t launch_t(const GemmArgs& g, cudaStream_t stream) {
 cudaError_t launch_bulk_zp(const GemmArgs& g, cudaStream_t stream) {
   const bool inter = g.layout == BQ_LAYOUT_INTERLEAVED;
   const bool full = g.K % GemvCfg<4>::STEP == 0;
+  if (g.M <= 8 && gemv_x_bytes<ACT_F16>(g.M, g.K) <= GEMV_XS_MAX) {   // activations staged in shared memory
+    if (full) return inter ? launch_bulk<4, ACT_F16, 1, true, true, true, true>(g, stream)
+                           : launch_bulk<4, ACT_F16, 1, false, true, true, true>(g, stream);
+    return inter ? launch_bulk<4, ACT_F16, 1, true, false, true, true>(g, stream)
+                 : launch_bulk<4, ACT_F16, 1, false, false, true, true>(g, stream);
+  }
   if (g.M <= 8) {
     if (full) return inter ? launch_bulk<4, ACT_F16, 1, true, true, false, true>(g, stream)
                            : launch_bulk<4, ACT_F16, 1, false, true, false, true>(g, stream);

@@ -55,8 +55,10 @@ def check_row_sum(rs, x):
 
 
 # M spans every bucket: the skinny kernel (M <= 16), the kernel with the weights as the MMA's A operand
-# (16 < M <= 128), the split-K single-CTA kernel and CTA pairs; ragged M and both layouts
-SHAPES = [(1, 4096, 4096, "interleaved"), (5, 1024, 512, "plain"), (17, 2048, 1024, "interleaved"),
+# (16 < M <= 128), the split-K single-CTA kernel and CTA pairs; ragged M and both layouts; K = 576 and
+# 448 end the skinny kernel's K steps (128) half way, where the lanes past K feed zeros to the row sums
+SHAPES = [(1, 4096, 4096, "interleaved"), (5, 1024, 512, "plain"), (3, 1024, 576, "plain"),
+          (16, 2048, 448, "interleaved"), (17, 2048, 1024, "interleaved"),
           (64, 11008, 4096, "interleaved"), (130, 4096, 2048, "plain"), (600, 8192, 512, "interleaved"),
           (1000, 4096, 1024, "plain")]
 
