@@ -213,10 +213,11 @@ __device__ __forceinline__ int exact_sum(float d0, float d1, int hd, float& l) {
 // DR: drain warp q's share of chunk c (k-blocks CH_KB c .. CH_KB (c + 1) - 1,
 // accumulated in accumulator c & 1): TMEM lane quadrant q (tile rows
 // 32q .. 32q + 31), every 32-column chunk of the tile.  Each accumulator value
-// is split as D = 8192 h + L, L is written back, and h is added to the running
-// high parts in the output's bytes (int16 for fp16 outputs, int32 for int32
-// outputs; the first drain writes them); then the warp arrives on the even
-// CTA's drained barrier of that accumulator.  If the chunk's barrier wait
+// is split as D = 8192 h + L (h = ceil(D / 8192), so -8192 < L <= 0), L is
+// written back, and h is added to the running high parts in the output's
+// bytes (int16 for fp16 outputs, int32 for int32 outputs; the first drain
+// writes them); then the warp arrives on the even CTA's drained barrier of
+// that accumulator.  If the chunk's barrier wait
 // gives up, the warp still arrives (the MMA issuer then finds the status).
 template <int BN>
 __device__ __forceinline__ void pair_drain(int c, uint32_t tmem, uint64_t* chunk_bar, uint64_t* drained_bar, int q,
@@ -465,7 +466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BBITS, BN, S
               tc_mma_f16_ts_pair(d, a_tm + 8 * kk, bdesc + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
           }
           tc_commit_pair(&empty_bar[s], 0x3);
-          // DR: the last k-block of a chunk whose accumulator a later chunk reuses: let the consumers drain it
+          // DR: the last k-block of a chunk whose accumulator a later chunk reuses: let the drain warps take it
           if (DR && (kb + 1) % CH_KB == 0 && chunk < ndrain) tc_commit_pair(&chunk_bar[chunk & 1], 0x3);
         }
         __syncwarp();
